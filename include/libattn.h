@@ -1,0 +1,223 @@
+/*
+ * libattn.h -- C ABI of libattn: masked exact attention with LSE output, LSE
+ * merge of chunked attention, paged KV append and paged GQA decode, as
+ * hand-written CUDA kernels for sm_103a (GB300).
+ *
+ * Conventions for every call
+ * --------------------------
+ * - Every data pointer is a DEVICE pointer on the current CUDA device; the
+ *   caller allocates and frees every buffer (outputs and workspace included).
+ *   The library never allocates, never frees, never synchronises, and only
+ *   enqueues work on the stream it is given.  Calls on one stream run in
+ *   order, so kv_append followed by paged_decode_attn on the same stream
+ *   attends over the appended token.
+ * - Arguments are validated on the host before anything is launched; a bad
+ *   argument returns ATTN_ERR_INVALID_ARG (or ATTN_ERR_UNSUPPORTED for a
+ *   valid but unimplemented shape/dtype) and enqueues nothing.
+ * - A failed launch returns ATTN_ERR_CUDA.
+ * - Errors found on the device (a block-table entry outside the cache, a
+ *   position beyond the table, a pipeline wait that timed out) are OR-ed into
+ *   a status word at the start of the caller's workspace and the offending
+ *   work is skipped (never read out of bounds, never hang).  The word is
+ *   sticky: read it with attn_check_device_status(), clear it with
+ *   attn_reset_device_status().  A workspace must be zero-filled once before
+ *   its first use.
+ * - Tensors are described by attn_tensor: element strides, innermost
+ *   dimension contiguous (stride 1).  Strides let the same call read the
+ *   contiguous [B, H, P, D] layout and the packed [T, H, D] layout (viewed
+ *   as [1, H, T, D] with strides {., D, H*D, 1}).
+ * - Thread safety: calls hold no global mutable state on the host; two calls
+ *   may run concurrently on different streams if their outputs and
+ *   workspaces do not overlap.
+ */
+#ifndef LIBATTN_H
+#define LIBATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h> /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum attn_status {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,    /* bad pointer, shape, stride or size       */
+    ATTN_ERR_UNSUPPORTED = 2,    /* valid, but no kernel for this shape/dtype */
+    ATTN_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed        */
+    ATTN_ERR_TIMEOUT = 4,        /* device: a pipeline wait gave up          */
+    ATTN_ERR_DEVICE_BOUNDS = 5,  /* device: table entry or position out of range */
+    ATTN_ERR_WORKSPACE = 6       /* workspace NULL, misaligned or too small  */
+} attn_status;
+
+typedef enum attn_dtype { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
+
+typedef struct attn_tensor {
+    void *data;          /* device pointer to element [0,...,0]          */
+    int32_t dtype;       /* attn_dtype                                   */
+    int32_t ndim;        /* number of used entries in shape/stride       */
+    int64_t shape[4];
+    int64_t stride[4];   /* element strides; stride[ndim-1] must be 1    */
+} attn_tensor;
+
+/* A paged KV cache: K and V each [num_blocks, num_kv_heads, block_size,
+ * head_dim], contiguous, bf16.  Token t of a sequence lives in physical
+ * block block_table[t / block_size] at slot t % block_size ("LLM inference
+ * memory accounting", section 15, paged KV cache). */
+typedef struct attn_kv_cache {
+    void *k;
+    void *v;
+    int32_t dtype;        /* ATTN_BF16 */
+    int32_t block_size;   /* tokens per block; 16 is implemented */
+    int64_t num_blocks;
+    int32_t num_kv_heads;
+    int32_t head_dim;     /* 64 or 128 */
+} attn_kv_cache;
+
+/* Bytes of workspace each call needs (always a multiple of 256).  The first
+ * 256 bytes hold the device status word. */
+size_t attn_fwd_workspace_size(void);
+size_t kv_append_workspace_size(void);
+size_t paged_decode_workspace_size(int32_t batch, int32_t num_q_heads,
+                                   int32_t max_blocks, int32_t block_size,
+                                   int32_t head_dim);
+
+/*
+ * attn_fwd -- exact masked scaled-dot-product attention with its softmax LSE.
+ *
+ * Defined by "MultiheadAttention fast path used 18 GB of VRAM" (TL;DR and the
+ * fix that routes padded inputs through SDPA with an additive -inf mask) and
+ * "[sglang] ROCm aiter ring attention" (section 1: the kernel also returns
+ * the log-sum-exp so chunk results can be merged).  For every batch b, query
+ * head h and query row i:
+ *     s_j  = scale * <q[b,h,i,:], k[b,g,j,:]> + key_pad_mask[b, j]
+ *     lse  = log(sum_j exp(s_j))                       (natural log)
+ *     out  = sum_j exp(s_j - lse) * v[b,g,j,:]
+ * with g = h / (Hq / Hkv) (grouped-query heads share a KV head).  The
+ * Hq x Pq x Pk score matrix is never stored: extra device memory is the
+ * output and LSE only.  A row whose keys are all masked yields out = 0 and
+ * lse = -inf.
+ *
+ *   q    [B, Hq, Pq, D]   bf16 or f32 (strided view)
+ *   k, v [B, Hkv, Pk, D]  same dtype as q
+ *   key_pad_mask  float32 additive mask, row b at key_pad_mask + b*mask_stride_b,
+ *                 Pk entries (0 keeps a key, -inf drops it; any finite value
+ *                 is added as is).  NULL means no mask.  This is the additive
+ *                 form: a boolean "True = padded" key_padding_mask must be
+ *                 converted by the caller (True -> -inf).
+ *   scale  multiplies q.k before the mask is added (usually 1/sqrt(D)).
+ *   out  [B, Hq, Pq, D]   bf16 or f32 (strided view), written in full.
+ *   lse  float32 [B, Hq, Pq] contiguous, or NULL.
+ * Implemented: bf16 with D in {64, 128} on the tensor cores (fp32
+ * accumulation and softmax); f32 with D <= 128, D % 4 == 0 on FP32 FMA (no
+ * TF32).  Pq, Pk >= 0 (zero-size calls do nothing but validate).
+ * Alignment: bf16 q/k/v base addresses and the strides of dims 0-2 must be
+ * multiples of 16 bytes.
+ */
+attn_status attn_fwd(const attn_tensor *q, const attn_tensor *k, const attn_tensor *v,
+                     const float *key_pad_mask, int64_t mask_stride_b, float scale,
+                     const attn_tensor *out, float *lse,
+                     void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * attn_lse_merge -- combine n attention results computed over disjoint KV
+ * chunks of the same queries.
+ *
+ * Defined by "[sglang] ROCm aiter ring attention" (section 1): with partial
+ * (out_i, lse_i), lse = log(sum_i exp(lse_i)) (evaluated with the maximum
+ * subtracted) and out = sum_i exp(lse_i - lse) * out_i; the accuracy section
+ * states that merging two chunks equals one call over all keys.  Partials
+ * with lse_i = -inf carry weight 0; if all are -inf, out = 0, lse = -inf.
+ *
+ *   n       number of partials, 1 <= n <= 8
+ *   outs    array of n tensors [B, H, P, D] (bf16 or f32, strided views)
+ *   lses    array of n float32 pointers, each [B, H, P] contiguous
+ *   out     [B, H, P, D] bf16 or f32; may alias outs[0] exactly (same
+ *           data pointer and strides), must not overlap the other outs
+ *   lse     float32 [B, H, P] contiguous, or NULL; must not overlap any lses[i]
+ * D <= 256, D % 8 == 0; bases and dim-0..2 strides 16-byte aligned.
+ */
+attn_status attn_lse_merge(int32_t n, const attn_tensor *outs, const float *const *lses,
+                           const attn_tensor *out, float *lse, cudaStream_t stream);
+
+/*
+ * kv_append -- write one new token's K and V per sequence into the paged
+ * cache ("KV cache in nanoVLM": after prefill, each decode step computes K/V
+ * for the newest token only and adds it to the cache).
+ *
+ * For every sequence b: blk = block_table[b*bt_stride + pos[b]/block_size],
+ * slot = pos[b] % block_size, and for every KV head g
+ *     cache.k[blk, g, slot, :] = k_new[b, g, :],  cache.v likewise.
+ * The copy is bit-exact.  pos[b] < 0 skips sequence b (an idle slot).
+ * A position past the table (pos[b]/block_size >= max_blocks) or a block id
+ * outside [0, num_blocks) sets ATTN_ERR_DEVICE_BOUNDS in the status word and
+ * skips that sequence.
+ *
+ *   block_table  int32 [batch, >= max_blocks] (row stride bt_stride)
+ *   pos          int32 [batch]
+ *   k_new, v_new [batch, num_kv_heads, head_dim] bf16 (strided views)
+ */
+attn_status kv_append(const attn_kv_cache *cache, const int32_t *block_table, int64_t bt_stride,
+                      int32_t max_blocks, const int32_t *pos,
+                      const attn_tensor *k_new, const attn_tensor *v_new,
+                      void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * paged_decode_attn -- one query token per sequence attends over its paged
+ * GQA cache ("KV cache in nanoVLM", attention step; "LLM inference memory
+ * accounting", sections 11 and 15: query heads share KV heads, and the cache
+ * is read through the block table).
+ *
+ * For every sequence b and query head h, with g = h / (Hq / Hkv) and
+ * L = ctx_lens[b] (the appended token included):
+ *     s_t = scale * <q[b,h,:], K[token t]>, t < L
+ *     out[b,h,:] = sum_t softmax(s)_t * V[token t],  lse[b,h] = log sum_t exp(s_t)
+ * where token t is read from block block_table[b*bt_stride + t/block_size],
+ * slot t % block_size.  L = 0 gives out = 0, lse = -inf.  A context needing
+ * more than max_blocks blocks, or a block id outside the cache, sets
+ * ATTN_ERR_DEVICE_BOUNDS and that (sequence, head) is written as zeros.
+ *
+ *   q       [batch, Hq, head_dim] bf16 (strided view)
+ *   out     [batch, Hq, head_dim] bf16 or f32
+ *   lse     float32 [batch, Hq] contiguous, or NULL
+ *   workspace >= paged_decode_workspace_size(batch, Hq, max_blocks,
+ *              block_size, head_dim) bytes: split-K partials, linear in
+ *              the longest possible context, never quadratic.
+ * Hq % Hkv == 0, Hq / Hkv <= 8.
+ */
+attn_status paged_decode_attn(const attn_tensor *q, const attn_kv_cache *cache,
+                              const int32_t *block_table, int64_t bt_stride, int32_t max_blocks,
+                              const int32_t *ctx_lens, float scale,
+                              const attn_tensor *out, float *lse,
+                              void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Test/debug export: gather the paged cache of every (sequence, KV head) into
+ * contiguous dst [batch, num_kv_heads, max_len, head_dim] (bf16), tokens
+ * t < lens[b]; rows t >= lens[b] are left untouched.  Bit-exact.
+ * which = 0 gathers K, 1 gathers V.  Same device-status rules as kv_append. */
+attn_status paged_kv_gather(const attn_kv_cache *cache, int32_t which,
+                            const int32_t *block_table, int64_t bt_stride, int32_t max_blocks,
+                            const int32_t *lens, int32_t batch, int64_t max_len, void *dst,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Copy the workspace's status word to the host (synchronises `stream`).
+ * Returns ATTN_OK or the lowest-numbered error recorded since the last reset;
+ * *raw (if not NULL) receives the full bit set, bit e meaning status e. */
+attn_status attn_check_device_status(const void *workspace, uint32_t *raw, cudaStream_t stream);
+
+/* Clear the status word (enqueued on `stream`). */
+attn_status attn_reset_device_status(void *workspace, cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *attn_status_string(attn_status status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int32_t attn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBATTN_H */

@@ -1,0 +1,318 @@
+"""Python binding of libattn (masked attention with LSE, LSE merge, paged KV
+append, paged GQA decode) for one GB300 GPU.
+
+This module only marshals arguments: it turns torch tensors into the C ABI's
+pointer/shape/stride descriptors (``include/libattn.h``) and calls the shared
+library through ctypes on the current CUDA stream.  Every step of the
+computation runs in the library's CUDA kernels; torch supplies device memory
+(outputs and workspaces the caller did not pass are allocated with it) and
+the stream.  There is no CPU fallback: if the library is missing or a call
+fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "load", "LibAttnError", "Workspace",
+    "attn_fwd", "attn_lse_merge", "kv_append", "paged_decode_attn", "paged_kv_gather",
+    "attn_fwd_workspace_size", "paged_decode_workspace_size", "check_device_status",
+]
+
+ATTN_F32, ATTN_BF16 = 0, 1
+_STATUS = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED", 3: "ATTN_ERR_CUDA",
+           4: "ATTN_ERR_TIMEOUT", 5: "ATTN_ERR_DEVICE_BOUNDS", 6: "ATTN_ERR_WORKSPACE"}
+
+
+class LibAttnError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        self.status = status
+        super().__init__(f"{call}: {_STATUS.get(status, status)}")
+
+
+class AttnTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+class AttnKVCache(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("dtype", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int64),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = False):
+    """Load libattn.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(f"libattn is not built ({path} missing); run "
+                                   "`python -c 'import __graft_entry__ as g; g.build()'`")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        P, I32, I64, SZ, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+        T = ctypes.POINTER(AttnTensor)
+        C = ctypes.POINTER(AttnKVCache)
+        sig = {
+            "attn_version": (I32, []),
+            "attn_status_string": (ctypes.c_char_p, [I32]),
+            "attn_fwd_workspace_size": (SZ, []),
+            "kv_append_workspace_size": (SZ, []),
+            "paged_decode_workspace_size": (SZ, [I32, I32, I32, I32, I32]),
+            "attn_fwd": (I32, [T, T, T, P, I64, F, T, P, P, SZ, P]),
+            "attn_lse_merge": (I32, [I32, T, ctypes.POINTER(P), T, P, P]),
+            "kv_append": (I32, [C, P, I64, I32, P, T, T, P, SZ, P]),
+            "paged_decode_attn": (I32, [T, C, P, I64, I32, P, F, T, P, P, SZ, P]),
+            "paged_kv_gather": (I32, [C, I32, P, I64, I32, P, I32, I64, P, P, SZ, P]),
+            "attn_check_device_status": (I32, [P, ctypes.POINTER(ctypes.c_uint32), P]),
+            "attn_reset_device_status": (I32, [P, P]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def exported_symbols() -> list[str]:
+    return ["attn_fwd", "attn_lse_merge", "kv_append", "paged_decode_attn", "paged_kv_gather",
+            "attn_fwd_workspace_size", "kv_append_workspace_size", "paged_decode_workspace_size",
+            "attn_check_device_status", "attn_reset_device_status", "attn_status_string", "attn_version"]
+
+
+# --------------------------------------------------------------------------
+# marshalling helpers
+# --------------------------------------------------------------------------
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype == torch.float32:
+        return ATTN_F32
+    raise TypeError(f"libattn takes bfloat16 or float32 tensors, got {t.dtype}")
+
+
+def _desc(t: torch.Tensor) -> AttnTensor:
+    if not t.is_cuda:
+        raise ValueError("libattn tensors must be on a CUDA device")
+    d = AttnTensor()
+    d.data = t.data_ptr()
+    d.dtype = _dtype_code(t)
+    d.ndim = t.dim()
+    for i in range(t.dim()):
+        d.shape[i] = t.shape[i]
+        d.stride[i] = t.stride(i)
+    return d
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(name: str, st: int):
+    if st != 0:
+        raise LibAttnError(name, st)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+class Workspace:
+    """A zero-initialised device buffer for the library's workspace argument
+    (its first word is the sticky device status)."""
+
+    def __init__(self, nbytes: int, device=None):
+        nbytes = max(256, (int(nbytes) + 255) // 256 * 256)
+        self.tensor = torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+        self.nbytes = nbytes
+
+    @property
+    def ptr(self) -> int:
+        return self.tensor.data_ptr()
+
+    def status(self, stream=None) -> int:
+        return check_device_status(self, stream)
+
+    def reset(self, stream=None):
+        _check("attn_reset_device_status", load().attn_reset_device_status(self.ptr, _stream(stream)))
+
+
+_default_ws: dict = {}
+
+
+def _small_ws(device) -> Workspace:
+    key = torch.device(device).index
+    ws = _default_ws.get(key)
+    if ws is None:
+        ws = Workspace(256, device=device)
+        _default_ws[key] = ws
+    return ws
+
+
+def check_device_status(ws: Workspace, stream=None) -> int:
+    raw = ctypes.c_uint32(0)
+    st = load().attn_check_device_status(ws.ptr, ctypes.byref(raw), _stream(stream))
+    return int(st)
+
+
+def attn_fwd_workspace_size() -> int:
+    return int(load().attn_fwd_workspace_size())
+
+
+def paged_decode_workspace_size(batch: int, num_q_heads: int, max_blocks: int, block_size: int = 16,
+                                head_dim: int = 128) -> int:
+    return int(load().paged_decode_workspace_size(batch, num_q_heads, max_blocks, block_size, head_dim))
+
+
+# --------------------------------------------------------------------------
+# the four calls
+# --------------------------------------------------------------------------
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, key_pad_mask: Optional[torch.Tensor] = None,
+             scale: Optional[float] = None, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+             return_lse: bool = True, workspace: Optional[Workspace] = None, stream=None):
+    """Masked exact attention; q [B, Hq, Pq, D], k/v [B, Hkv, Pk, D] (any
+    strides with a contiguous last dim, e.g. packed [T, H, D] permuted to
+    [1, H, T, D]).  key_pad_mask: float32 [B, Pk] additive (0 / -inf).
+    Returns (out, lse) with lse float32 [B, Hq, Pq] (or out alone)."""
+    lib = load()
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    if lse is not None:
+        assert lse.dtype == torch.float32 and lse.is_contiguous() and tuple(lse.shape) == tuple(q.shape[:3])
+    mptr, mstride = None, 0
+    if key_pad_mask is not None:
+        assert key_pad_mask.dtype == torch.float32 and key_pad_mask.stride(-1) == 1
+        mptr, mstride = key_pad_mask.data_ptr(), key_pad_mask.stride(0)
+    ws = workspace or _small_ws(q.device)
+    dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
+    st = lib.attn_fwd(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), mptr, mstride, float(scale),
+                      ctypes.byref(do), _ptr(lse), ws.ptr, ws.nbytes, _stream(stream))
+    _check("attn_fwd", st)
+    return (out, lse) if return_lse else out
+
+
+def attn_lse_merge(outs: Sequence[torch.Tensor], lses: Sequence[torch.Tensor], out: Optional[torch.Tensor] = None,
+                   lse: Optional[torch.Tensor] = None, stream=None):
+    """Merge chunk results: lse = log sum_i exp(lse_i), out = sum_i exp(lse_i - lse) out_i."""
+    lib = load()
+    n = len(outs)
+    if out is None:
+        out = torch.empty(outs[0].shape, dtype=outs[0].dtype, device=outs[0].device)
+    if lse is None:
+        lse = torch.empty(lses[0].shape, dtype=torch.float32, device=outs[0].device)
+    arr = (AttnTensor * n)(*[_desc(o) for o in outs])
+    for l in lses:
+        assert l.dtype == torch.float32 and l.is_contiguous()
+    lptrs = (ctypes.c_void_p * n)(*[l.data_ptr() for l in lses])
+    do = _desc(out)
+    st = lib.attn_lse_merge(n, arr, lptrs, ctypes.byref(do), _ptr(lse), _stream(stream))
+    _check("attn_lse_merge", st)
+    return out, lse
+
+
+def _cache(k_cache: torch.Tensor, v_cache: torch.Tensor) -> AttnKVCache:
+    assert k_cache.shape == v_cache.shape and k_cache.is_contiguous() and v_cache.is_contiguous()
+    c = AttnKVCache()
+    c.k = k_cache.data_ptr()
+    c.v = v_cache.data_ptr()
+    c.dtype = _dtype_code(k_cache)
+    c.num_blocks = k_cache.shape[0]
+    c.num_kv_heads = k_cache.shape[1]
+    c.block_size = k_cache.shape[2]
+    c.head_dim = k_cache.shape[3]
+    return c
+
+
+def kv_append(k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor, pos: torch.Tensor,
+              k_new: torch.Tensor, v_new: torch.Tensor, workspace: Optional[Workspace] = None, stream=None):
+    """Write k_new/v_new [B, Hkv, D] at token position pos[b] of each
+    sequence's paged cache (caches [num_blocks, Hkv, block_size, D])."""
+    lib = load()
+    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1
+    assert pos.dtype == torch.int32 and pos.is_contiguous()
+    ws = workspace or _small_ws(k_cache.device)
+    c = _cache(k_cache, v_cache)
+    dk, dv = _desc(k_new), _desc(v_new)
+    st = lib.kv_append(ctypes.byref(c), block_table.data_ptr(), block_table.stride(0), block_table.shape[1],
+                       pos.data_ptr(), ctypes.byref(dk), ctypes.byref(dv), ws.ptr, ws.nbytes, _stream(stream))
+    _check("kv_append", st)
+
+
+def paged_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
+                      ctx_lens: torch.Tensor, scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                      lse: Optional[torch.Tensor] = None, return_lse: bool = False,
+                      workspace: Optional[Workspace] = None, stream=None):
+    """One query token per sequence, q [B, Hq, D], over the paged cache;
+    ctx_lens int32 [B] counts the attended tokens (the appended one included)."""
+    lib = load()
+    B, Hq, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1
+    assert ctx_lens.dtype == torch.int32 and ctx_lens.is_contiguous()
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    max_blocks = block_table.shape[1]
+    need = paged_decode_workspace_size(B, Hq, max_blocks, k_cache.shape[2], D)
+    ws = workspace
+    if ws is None or ws.nbytes < need:
+        ws = Workspace(need, device=q.device)
+    c = _cache(k_cache, v_cache)
+    dq, do = _desc(q), _desc(out)
+    st = lib.paged_decode_attn(ctypes.byref(dq), ctypes.byref(c), block_table.data_ptr(), block_table.stride(0),
+                               max_blocks, ctx_lens.data_ptr(), float(scale), ctypes.byref(do), _ptr(lse),
+                               ws.ptr, ws.nbytes, _stream(stream))
+    _check("paged_decode_attn", st)
+    return (out, lse) if return_lse else out
+
+
+def paged_kv_gather(cache: torch.Tensor, block_table: torch.Tensor, lens: torch.Tensor, max_len: int,
+                    out: Optional[torch.Tensor] = None, workspace: Optional[Workspace] = None,
+                    stream=None) -> torch.Tensor:
+    """Contiguous copy [B, Hkv, max_len, D] of the first lens[b] tokens of each
+    sequence in one paged cache tensor (K or V); rows past lens[b] untouched."""
+    lib = load()
+    B = lens.shape[0]
+    nb, Hkv, bs, D = cache.shape
+    assert lens.dtype == torch.int32 and lens.is_contiguous()
+    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1
+    if out is None:
+        out = torch.zeros((B, Hkv, max_len, D), dtype=cache.dtype, device=cache.device)
+    c = _cache(cache, cache)
+    ws = workspace or _small_ws(cache.device)
+    st = lib.paged_kv_gather(ctypes.byref(c), 0, block_table.data_ptr(), block_table.stride(0),
+                             block_table.shape[1], lens.data_ptr(), B, max_len, out.data_ptr(), ws.ptr, ws.nbytes,
+                             _stream(stream))
+    _check("paged_kv_gather", st)
+    return out

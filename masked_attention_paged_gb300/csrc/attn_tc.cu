@@ -1,0 +1,505 @@
+// attn_tc.cu -- masked exact attention with LSE on the 5th-generation tensor
+// cores (tcgen05 + TMEM + TMA), bf16 inputs, fp32 accumulation and softmax.
+//
+// What it computes ("MultiheadAttention fast path used 18 GB of VRAM", the
+// SDPA route with an additive -inf padding mask; "[sglang] ROCm aiter ring
+// attention", section 1, the LSE the merge needs): for each query row
+//   s_j = scale * q.k_j + mask_j,  out = sum_j softmax(s)_j v_j,  lse = log sum_j e^{s_j}
+// without ever storing the score matrix: one 128 x 128 score tile lives in
+// tensor memory at a time and is folded into the running output with the
+// online-softmax rescale.
+//
+// CTA = one 128-row query tile of one (batch, head); 6 warps:
+//   warp 0      TMA producer: Q once, then K_j / V_j tiles into a ring of
+//               shared-memory stages (128-byte swizzle, 4-D tensor maps so the
+//               same code reads [B,H,P,D] and packed [T,H,D] layouts).
+//   warp 1      allocates TMEM; one lane issues tcgen05.mma:
+//                 S_j = Q K_j^T  (M=128, N=128, K=D)  into TMEM S[j%2]
+//                 O  += P_j V_j  (M=128, N=D,   K=128) into TMEM O
+//               and signals completion with tcgen05.commit -> mbarrier.
+//   warps 2-5   softmax: thread r owns row r (TMEM lane r).  Reads its S row
+//               from TMEM, adds the mask, keeps the running max/sum in the
+//               log2 domain, rescales O in TMEM when the max grows, writes
+//               P (bf16) to shared memory in the UMMA K-major swizzled layout,
+//               and finally normalises O and writes out / lse.
+// Order on the tensor pipe: S_0, S_1, PV_0, S_2, PV_1, ... so the softmax of
+// tile j+1 overlaps the PV of tile j.
+//
+// Every wait is bounded (common.cuh): a hang turns into ATTN_ERR_TIMEOUT in
+// the caller's status word and the CTA winds down and frees its TMEM.
+#include <cuda.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace attn {
+namespace {
+
+constexpr int kBM = 128;       // query rows per CTA tile
+constexpr int kBN = 128;       // keys per KV tile
+constexpr int kThreads = 192;  // 6 warps
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+constexpr int kBoxBytes = kBM * 128;  // one 64-column (128-byte) box of 128 rows
+
+template <int D>
+struct Cfg {
+  static constexpr int kBoxes = D / 64;
+  static constexpr int kTileBytes = kBM * D * 2;
+  static constexpr int kStages = (D == 64) ? 3 : 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffP = kOffV + kStages * kTileBytes;
+  static constexpr int kOffMask = kOffP + kBM * kBN * 2;
+  static constexpr int kOffBar = kOffMask + 2 * kBN * 4;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + slack to align the base to 1024
+};
+
+struct Barriers {
+  uint64_t q_full;
+  uint64_t k_full[3], k_empty[3];
+  uint64_t v_full[3], v_empty[3];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full, o_done, drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct TmaCoordMap {
+  // which tensor-map coordinate slot (1..3) carries the row, head and batch index
+  int slot_p, slot_h, slot_b;
+};
+
+struct TcParams {
+  int Pq, Pk, Hq, group, n_kv_tiles;
+  float scale_log2;
+  const float* mask;
+  int64_t mask_stride;
+  void* out;
+  int64_t out_stride[3];  // b, h, row (elements)
+  float* lse;
+  uint32_t* status;
+  TmaCoordMap cq, ck, cv;
+};
+
+__device__ __forceinline__ void coords(const TmaCoordMap& m, int p, int h, int b, int& c1, int& c2, int& c3) {
+  c1 = m.slot_p == 1 ? p : (m.slot_h == 1 ? h : b);
+  c2 = m.slot_p == 2 ? p : (m.slot_h == 2 ? h : b);
+  c3 = m.slot_p == 3 ? p : (m.slot_h == 3 ? h : b);
+}
+
+template <int D, bool OUT_BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
+  using C = Cfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Barriers* bars = reinterpret_cast<Barriers*>(smem + C::kOffBar);
+  float* mask_buf = reinterpret_cast<float*>(smem + C::kOffMask);  // [2][kBN], log2 domain
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int q_tile = blockIdx.x;
+  const int h = blockIdx.y;
+  const int b = blockIdx.z;
+  const int g = h / prm.group;
+  const int q0 = q_tile * kBM;
+  const int nkv = prm.n_kv_tiles;
+  volatile int* abort = &bars->abort;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->q_full, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars->k_full[s], 1);
+      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->v_full[s], 1);
+      mbar_init(&bars->v_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->s_free[i], 4);
+    }
+    mbar_init(&bars->p_full, 4);
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->drain, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      int c1, c2, c3;
+      mbar_arrive_expect_tx(&bars->q_full, C::kTileBytes);
+      coords(prm.cq, q0, h, b, c1, c2, c3);
+#pragma unroll
+      for (int x = 0; x < C::kBoxes; ++x)
+        tma_load_4d(smem + C::kOffQ + x * kBoxBytes, &tm_q, &bars->q_full, x * 64, c1, c2, c3);
+      int k_issued = 0, v_issued = 0;
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % C::kStages;
+        const uint32_t ph = (j / C::kStages) & 1;
+        if (!mbar_wait(&bars->k_empty[s], ph ^ 1, abort, prm.status)) break;
+        mbar_arrive_expect_tx(&bars->k_full[s], C::kTileBytes);
+        coords(prm.ck, j * kBN, g, b, c1, c2, c3);
+#pragma unroll
+        for (int x = 0; x < C::kBoxes; ++x)
+          tma_load_4d(smem + C::kOffK + s * C::kTileBytes + x * kBoxBytes, &tm_k, &bars->k_full[s], x * 64,
+                      c1, c2, c3);
+        k_issued = j + 1;
+        if (!mbar_wait(&bars->v_empty[s], ph ^ 1, abort, prm.status)) break;
+        mbar_arrive_expect_tx(&bars->v_full[s], C::kTileBytes);
+        coords(prm.cv, j * kBN, g, b, c1, c2, c3);
+#pragma unroll
+        for (int x = 0; x < C::kBoxes; ++x)
+          tma_load_4d(smem + C::kOffV + s * C::kTileBytes + x * kBoxBytes, &tm_v, &bars->v_full[s], x * 64,
+                      c1, c2, c3);
+        v_issued = j + 1;
+      }
+      if (*abort) {
+        // let every copy still in flight land before the CTA exits
+        drain_wait(&bars->q_full, 0);
+        for (int j = (k_issued > C::kStages ? k_issued - C::kStages : 0); j < k_issued; ++j)
+          drain_wait(&bars->k_full[j % C::kStages], (j / C::kStages) & 1);
+        for (int j = (v_issued > C::kStages ? v_issued - C::kStages : 0); j < v_issued; ++j)
+          drain_wait(&bars->v_full[j % C::kStages], (j / C::kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);
+      constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
+      const uint32_t q_addr = smem_u32(smem + C::kOffQ);
+      const uint32_t p_addr = smem_u32(smem + C::kOffP);
+      bool ok = mbar_wait(&bars->q_full, 0, abort, prm.status);
+      tc_fence_after();
+      auto issue_pv = [&](int t) -> bool {
+        const int s = t % C::kStages;
+        const uint32_t ph = (t / C::kStages) & 1;
+        if (!mbar_wait(&bars->p_full, t & 1, abort, prm.status)) return false;
+        if (!mbar_wait(&bars->v_full[s], ph, abort, prm.status)) return false;
+        tc_fence_after();
+        const uint32_t v_addr = smem_u32(smem + C::kOffV + s * C::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          // A = P: K-major, 64-key column blocks of 16 KB, 32 bytes per k-step
+          const uint64_t a = sdesc_sw128(p_addr + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
+          // B = V: MN-major (d contiguous); 16 keys = two 8-row groups (SBO),
+          // next 64-column box of d at LBO
+          const uint64_t bd = sdesc_sw128(v_addr + kk * 2048, kBoxBytes, 1024);
+          umma_bf16_ss(tmem + kColO, a, bd, idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(&bars->o_done);
+        umma_commit(&bars->v_empty[s]);
+        return true;
+      };
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int s = j % C::kStages;
+        const uint32_t ph = (j / C::kStages) & 1;
+        const int sb = j & 1;
+        if (!mbar_wait(&bars->k_full[s], ph, abort, prm.status)) { ok = false; break; }
+        if (j >= 2 && !mbar_wait(&bars->s_free[sb], ((j >> 1) & 1) ^ 1, abort, prm.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(smem + C::kOffK + s * C::kTileBytes);
+        const uint32_t s_col = sb ? kColS1 : kColS0;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+          const uint64_t a = sdesc_sw128(q_addr + off, 16, 1024);
+          const uint64_t bk = sdesc_sw128(k_addr + off, 16, 1024);
+          umma_bf16_ss(tmem + s_col, a, bk, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&bars->s_full[sb]);
+        umma_commit(&bars->k_empty[s]);
+        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok && nkv > 0) issue_pv(nkv - 1);
+      // every MMA this thread issued must finish before TMEM is released
+      umma_commit(&bars->drain);
+      drain_wait(&bars->drain, 0);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int wg_tid = threadIdx.x - 64;  // 0..127
+    const int quarter = warp & 3;         // TMEM lanes this warp may touch
+    const int row = quarter * 32 + lane;  // row within the tile == TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const float kLog2e = 1.4426950408889634f;
+    const float* mrow = prm.mask ? prm.mask + static_cast<int64_t>(b) * prm.mask_stride : nullptr;
+    auto mask_at = [&](int key) -> float {
+      if (key >= prm.Pk) return -INFINITY;
+      return mrow ? mrow[key] * kLog2e : 0.0f;
+    };
+    float m_run = -INFINITY;  // running max, log2 units
+    float l_run = 0.0f;       // running sum of 2^(x - m_run)
+    float mreg = nkv > 0 ? mask_at(wg_tid) : 0.0f;
+    uint8_t* p_smem = smem + C::kOffP;
+    bool ok = true;
+
+    for (int j = 0; j < nkv; ++j) {
+      const int sb = j & 1;
+      mask_buf[sb * kBN + wg_tid] = mreg;
+      named_bar_sync(1, 128);
+      if (j + 1 < nkv) mreg = mask_at((j + 1) * kBN + wg_tid);
+      // wait outcomes are made warp-uniform: tcgen05.ld/st need the whole warp
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j >> 1) & 1, abort, prm.status))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[4][32];
+      const uint32_t s_col = sb ? kColS1 : kColS0;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_addr + s_col + c * 32, sr[c]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->s_free[sb]);
+
+      // logits in log2 units with the additive mask (in place), tile max
+      float mt = -INFINITY;
+      const float4* mb = reinterpret_cast<const float4*>(mask_buf + sb * kBN);
+#pragma unroll
+      for (int c4 = 0; c4 < kBN / 4; ++c4) {
+        const float4 mv = mb[c4];
+        const float madd[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c = 4 * c4 + e;
+          const float xv = fmaf(__uint_as_float(sr[c >> 5][c & 31]), prm.scale_log2, madd[e]);
+          sr[c >> 5][c & 31] = __float_as_uint(xv);
+          mt = fmaxf(mt, xv);
+        }
+      }
+      const float m_new = fmaxf(m_run, mt);
+      const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+      const float alpha = fast_exp2(m_run - m_use);  // 0 while nothing was unmasked
+      float rs = 0.0f;
+#pragma unroll
+      for (int c = 0; c < kBN; ++c) {
+        const float pv = fast_exp2(__uint_as_float(sr[c >> 5][c & 31]) - m_use);
+        sr[c >> 5][c & 31] = __float_as_uint(pv);
+        rs += pv;
+      }
+      l_run = l_run * alpha + rs;
+      m_run = m_new;
+
+      if (j > 0) {
+        // PV_{j-1} must be done: O is stable and the P buffer is free
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_done, (j - 1) & 1, abort, prm.status))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tmem + lane_addr + kColO + c * 32, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(tmem + lane_addr + kColO + c * 32, o);
+          }
+          tmem_wait_st();
+        }
+      }
+      // P (bf16) into the swizzled K-major operand layout: key chunk c of 8
+      // keys -> column block c/8, 16-byte slot (c%8) ^ (row%8) of the row
+#pragma unroll
+      for (int c = 0; c < kBN / 8; ++c) {
+        const uint32_t* pr = &sr[c >> 2][(c & 3) * 8];
+        uint4 w;
+        w.x = pack_bf16x2(__uint_as_float(pr[0]), __uint_as_float(pr[1]));
+        w.y = pack_bf16x2(__uint_as_float(pr[2]), __uint_as_float(pr[3]));
+        w.z = pack_bf16x2(__uint_as_float(pr[4]), __uint_as_float(pr[5]));
+        w.w = pack_bf16x2(__uint_as_float(pr[6]), __uint_as_float(pr[7]));
+        uint8_t* dst = p_smem + (c >> 3) * kBoxBytes + row * 128 + ((((c & 7) ^ (row & 7))) << 4);
+        *reinterpret_cast<uint4*>(dst) = w;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_full);
+    }
+
+    // ---------------------------------------------------------- epilogue
+    if (ok && nkv > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done, (nkv - 1) & 1, abort, prm.status));
+      tc_fence_after();
+    }
+    const int qi = q0 + row;
+    const bool empty = !(l_run > 0.0f);
+    const float inv_l = empty ? 0.0f : 1.0f / l_run;
+    const int64_t obase = static_cast<int64_t>(b) * prm.out_stride[0] + static_cast<int64_t>(h) * prm.out_stride[1] +
+                          static_cast<int64_t>(qi) * prm.out_stride[2];
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      if (ok && nkv > 0) {
+        tmem_ld32(tmem + lane_addr + kColO + c * 32, o);
+        tmem_wait_ld(o);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = 0u;
+      }
+      if (qi < prm.Pq && ok) {
+        if constexpr (OUT_BF16) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(prm.out) + obase + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l);
+            dst[i] = w;
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(prm.out) + obase + c * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(o[4 * i + 0]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                 __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+        }
+      }
+    }
+    if (prm.lse != nullptr && qi < prm.Pq && ok) {
+      const float lse2 = empty ? -INFINITY : (m_run + __log2f(l_run));
+      prm.lse[(static_cast<int64_t>(b) * prm.Hq + h) * prm.Pq + qi] = lse2 * 0.6931471805599453f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// A 4-D bf16 tensor map over a [B, H, P, D] view whose row/head/batch
+// strides may come in any order (contiguous or packed [T, H, D]).  The
+// three outer dimensions are ordered by increasing stride; `cm` records which
+// coordinate slot carries which index.  Box: 64 columns x 128 rows, 128-byte
+// swizzle, zero fill outside the tensor.
+bool make_map(CUtensorMap* map, TmaCoordMap* cm, const View4& t) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  struct Dim {
+    int64_t size, stride;
+    int which;  // 0 = row (P), 1 = head, 2 = batch
+  } d[3] = {{t.shape[2], t.stride[2], 0}, {t.shape[1], t.stride[1], 1}, {t.shape[0], t.stride[0], 2}};
+  // a dimension of extent 1 has no meaningful stride: give it a valid one
+  for (auto& x : d)
+    if (x.size <= 1) x.stride = int64_t(1) << 30;
+  for (int i = 0; i < 3; ++i)
+    for (int j = i + 1; j < 3; ++j)
+      if (d[j].stride < d[i].stride || (d[j].stride == d[i].stride && d[j].which < d[i].which)) {
+        Dim tmp = d[i];
+        d[i] = d[j];
+        d[j] = tmp;
+      }
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(t.shape[3]), 0, 0, 0};
+  cuuint64_t strides[3];
+  cuuint32_t box[4] = {64, 1, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  for (int i = 0; i < 3; ++i) {
+    dims[i + 1] = static_cast<cuuint64_t>(d[i].size < 1 ? 1 : d[i].size);
+    strides[i] = static_cast<cuuint64_t>(d[i].stride) * 2;
+    if (d[i].which == 0) {
+      box[i + 1] = kBM;
+      cm->slot_p = i + 1;
+    } else if (d[i].which == 1) {
+      cm->slot_h = i + 1;
+    } else {
+      cm->slot_b = i + 1;
+    }
+  }
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t.data, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D, bool OUT_BF16>
+cudaError_t launch_tc(const AttnFwdArgs& a, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  TcParams p;
+  if (!make_map(&mq, &p.cq, a.q) || !make_map(&mk, &p.ck, a.k) || !make_map(&mv, &p.cv, a.v))
+    return cudaErrorInvalidValue;
+  p.Pq = static_cast<int>(a.Pq);
+  p.Pk = static_cast<int>(a.Pk);
+  p.Hq = static_cast<int>(a.Hq);
+  p.group = static_cast<int>(a.Hq / a.Hkv);
+  p.n_kv_tiles = static_cast<int>((a.Pk + kBN - 1) / kBN);
+  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  p.mask = a.mask;
+  p.mask_stride = a.mask_stride;
+  p.out = a.out.data;
+  p.out_stride[0] = a.out.stride[0];
+  p.out_stride[1] = a.out.stride[1];
+  p.out_stride[2] = a.out.stride[2];
+  p.lse = a.lse;
+  p.status = a.status;
+  auto kern = attn_fwd_tc_kernel<D, OUT_BF16>;
+  const int smem = Cfg<D>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(static_cast<unsigned>((a.Pq + kBM - 1) / kBM), static_cast<unsigned>(a.Hq),
+            static_cast<unsigned>(a.B));
+  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd_tc(const AttnFwdArgs& a, cudaStream_t stream) {
+  const bool bf16_out = a.out.dtype == ATTN_BF16;
+  if (a.D == 64) return bf16_out ? launch_tc<64, true>(a, stream) : launch_tc<64, false>(a, stream);
+  if (a.D == 128) return bf16_out ? launch_tc<128, true>(a, stream) : launch_tc<128, false>(a, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

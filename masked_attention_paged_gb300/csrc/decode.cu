@@ -1,0 +1,457 @@
+// decode.cu -- paged GQA decode: one query token per sequence attends over
+// its paged KV cache ("KV cache in nanoVLM", the attention step of each
+// decode iteration; "LLM inference memory accounting", sections 11 and 15:
+// query heads share KV heads, and the cache is read through a block table).
+//
+// The work is HBM-bound (about 4 flops per KV byte), so this is an FMA
+// kernel organised around the bytes:
+//  * split-K over the context: CTA (split s, KV head g, sequence b) covers
+//    tokens [512 s, 512 (s+1)) and all G = Hq/Hkv query heads of the group,
+//    so every K/V byte is read from HBM once;
+//  * each of the 4 warps walks every 4th 16-token block of the split; lane 0
+//    streams the block's K and V (4 KB each at D = 128) with 1-D bulk copies
+//    into a per-warp double buffer, the block ids prefetched from the table;
+//  * lane l owns 8 consecutive dims (one 16-byte chunk) of a subset of the
+//    block's tokens; dot products are reduced with a transposing shuffle
+//    tree that leaves each lane a few (head, token) scores; the online
+//    softmax keeps per-head running max/sum in log2 units with lazy rescale;
+//  * the split's (output, LSE) goes to the workspace and a second kernel
+//    merges the splits with the LSE rule of the ring-attention page.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace attn {
+
+int decode_num_splits(int max_blocks, int block_size) {
+  const int64_t tokens = static_cast<int64_t>(max_blocks) * block_size;
+  return static_cast<int>((tokens + kDecodeSplitTokens - 1) / kDecodeSplitTokens);
+}
+
+size_t decode_partial_bytes(int64_t B, int64_t Hq, int n_split, int D) {
+  const size_t n = static_cast<size_t>(B) * Hq * n_split;
+  size_t bytes = n * D * sizeof(float) + n * sizeof(float);
+  return (bytes + 255) & ~size_t(255);
+}
+
+namespace {
+
+constexpr int kBS = 16;                             // tokens per cache block
+constexpr int kWarps = 4;
+constexpr int kStages = 2;                          // per-warp buffer depth
+constexpr float kLazyRescale = 8.0f;                // log2 units of headroom before a rescale
+
+struct DecodeParams {
+  const uint16_t* kc;
+  const uint16_t* vc;
+  int64_t num_blocks;
+  int Hkv;
+  const uint16_t* q;
+  int64_t q_stride[2];  // batch, head
+  const int32_t* bt;
+  int64_t bt_stride;
+  int max_blocks;
+  const int32_t* ctx_lens;
+  float scale_log2;
+  float* o_part;    // [B, Hq, n_split, D]
+  float* lse_part;  // [B, Hq, n_split], log2 units
+  int n_split;
+  int Hq;
+  uint32_t* status;
+};
+
+template <int D, int G>
+struct Geo {
+  static constexpr int CPR = D / 8;             // 16-byte chunks per token row = lanes per token set
+  static constexpr int TS = 32 / CPR;           // token sets per warp
+  static constexpr int TPL = kBS / TS;          // tokens per lane per block
+  static constexpr int N = G * TPL;             // partial dot products per lane
+  static constexpr int R = N >= CPR ? N / CPR : 1;  // scores a lane keeps after the reduce
+  static constexpr int SHARE = N >= CPR ? 1 : CPR / N;  // lanes holding the same score
+  static constexpr int HEAD_LANES = CPR / G;    // lanes of one token set holding one head
+  static constexpr int BLOCK_BYTES = kBS * D * 2;
+};
+
+template <int D, int G>
+__global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeParams p) {
+  using Gm = Geo<D, G>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  // per warp: kStages x {K block, V block}
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * 2 * Gm::BLOCK_BYTES);
+  float* comb = reinterpret_cast<float*>(bars + kWarps * kStages);  // [kWarps][G][D + 2]
+
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int cl = lane % Gm::CPR;  // chunk column
+  const int ts = lane / Gm::CPR;  // token set
+  int L = p.ctx_lens[b];
+  if (L < 0) L = 0;
+  if (L > p.max_blocks * kBS) {
+    if (threadIdx.x == 0 && split == 0) report(p.status, kStatusBounds);
+    L = p.max_blocks * kBS;
+  }
+  const int t_begin = split * kDecodeSplitTokens;
+  if (t_begin >= L) return;  // nothing of this sequence in this split
+  const int t_end = min(L, t_begin + kDecodeSplitTokens);
+  const int nblk = (t_end - t_begin + kBS - 1) / kBS;
+  const int lb0 = t_begin / kBS;
+
+  uint8_t* wbuf = smem + warp * kStages * 2 * Gm::BLOCK_BYTES;
+  uint64_t* wbar = bars + warp * kStages;
+  if (lane == 0)
+    for (int s = 0; s < kStages; ++s) mbar_init(&wbar[s], 1);
+  fence_mbar_init();
+  __syncwarp();
+
+  // this warp's blocks: i-th is lb0 + warp + kWarps*i; lane i prefetches its id
+  const int my_n = nblk > warp ? (nblk - warp + kWarps - 1) / kWarps : 0;
+  int my_blk = -1;
+  if (lane < my_n) {
+    my_blk = p.bt[static_cast<int64_t>(b) * p.bt_stride + lb0 + warp + kWarps * lane];
+    if (my_blk < 0 || my_blk >= p.num_blocks) {
+      report(p.status, kStatusBounds);
+      my_blk = -1;
+    }
+  }
+  // lane 0: start the copy of this warp's i-th block (its id already broadcast)
+  auto issue = [&](int i, int blk) {
+    const int s = i % kStages;
+    if (blk < 0) {  // bad id: complete the phase without data; the block is skipped
+      mbar_arrive(&wbar[s]);
+      return;
+    }
+    uint8_t* dst = wbuf + s * 2 * Gm::BLOCK_BYTES;
+    const int64_t off = (static_cast<int64_t>(blk) * p.Hkv + g) * (kBS * D);
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(&wbar[s], 2 * Gm::BLOCK_BYTES);
+    bulk_load(dst, p.kc + off, Gm::BLOCK_BYTES, &wbar[s]);
+    bulk_load(dst + Gm::BLOCK_BYTES, p.vc + off, Gm::BLOCK_BYTES, &wbar[s]);
+  };
+
+  // q of this lane's 8 dims for every head of the group, pre-scaled to log2 units
+  float qf[G][8];
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh) {
+    const int h = g * G + hh;
+    const uint4 w = *reinterpret_cast<const uint4*>(p.q + b * p.q_stride[0] + h * p.q_stride[1] + cl * 8);
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      qf[hh][2 * e] = bf16lo_to_f32(wv[e]) * p.scale_log2;
+      qf[hh][2 * e + 1] = bf16hi_to_f32(wv[e]) * p.scale_log2;
+    }
+  }
+  float o[G][8];
+  float m_run[G];
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh) {
+    m_run[hh] = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[hh][e] = 0.f;
+  }
+  // after the reduce this lane keeps scores idx = k + R * (cl / SHARE), k < R,
+  // of the list idx = head * TPL + i (token TS * i + ts of the block)
+  const int my_idx0 = Gm::R * (cl / Gm::SHARE);
+  const int my_head = my_idx0 / Gm::TPL;
+  const bool counts_sum = (cl % Gm::SHARE) == 0;  // one of the lanes sharing a score adds it
+  float l_part = 0.f;
+
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) abort_flag = 0;
+  __syncthreads();
+  bool ok = true;
+  int issued = 0;
+  // prologue: every lane takes part in the broadcast, lane 0 issues
+  for (int i = 0; i < kStages && i < my_n; ++i) {
+    const int blk = __shfl_sync(0xffffffffu, my_blk, i);
+    if (lane == 0) issue(i, blk);
+    issued = i + 1;
+  }
+
+  for (int i = 0; i < my_n; ++i) {
+    const int s = i % kStages;
+    const int blk = __shfl_sync(0xffffffffu, my_blk, i);
+    const bool landed = mbar_wait(&wbar[s], (i / kStages) & 1, &abort_flag, p.status);
+    if (!__all_sync(0xffffffffu, landed)) {  // leave together: the shuffles below need every lane
+      ok = false;
+      break;
+    }
+    if (blk >= 0) {
+      const uint8_t* kb = wbuf + s * 2 * Gm::BLOCK_BYTES;
+      const uint8_t* vb = kb + Gm::BLOCK_BYTES;
+      const int tok0 = (lb0 + warp + kWarps * i) * kBS;  // first token of the block
+
+      // partial dot products over this lane's 8 dims
+      float acc[Gm::N];
+#pragma unroll
+      for (int i2 = 0; i2 < Gm::TPL; ++i2) {
+        const int t = Gm::TS * i2 + ts;
+        const uint4 kw = *reinterpret_cast<const uint4*>(kb + t * (D * 2) + cl * 16);
+        const float kf[8] = {bf16lo_to_f32(kw.x), bf16hi_to_f32(kw.x), bf16lo_to_f32(kw.y), bf16hi_to_f32(kw.y),
+                             bf16lo_to_f32(kw.z), bf16hi_to_f32(kw.z), bf16lo_to_f32(kw.w), bf16hi_to_f32(kw.w)};
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+          float a = qf[hh][0] * kf[0];
+#pragma unroll
+          for (int e = 1; e < 8; ++e) a = fmaf(qf[hh][e], kf[e], a);
+          acc[hh * Gm::TPL + i2] = a;
+        }
+      }
+      // transposing reduce over the CPR lanes of a token set: each stage
+      // halves the list a lane carries and sums it with its partner's half
+#pragma unroll
+      for (int st = 0; (Gm::CPR >> (st + 1)) >= 1; ++st) {
+        const int mask = Gm::CPR >> (st + 1);
+        const int cur = Gm::N >> st;
+        if (cur > 1) {
+          const int half = cur >> 1;
+          const bool upper = (cl & mask) != 0;
+#pragma unroll
+          for (int k = 0; k < half; ++k) {
+            const float send = upper ? acc[k] : acc[k + half];
+            const float keep = upper ? acc[k + half] : acc[k];
+            acc[k] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+          }
+        } else {
+          acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], mask);
+        }
+      }
+      // scores kept by this lane; tokens past the context are masked
+      float sc[Gm::R];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < Gm::R; ++k) {
+        const int idx = my_idx0 + k;
+        const int t = Gm::TS * (idx % Gm::TPL) + ts;
+        sc[k] = (tok0 + t < t_end) ? acc[k] : -INFINITY;
+        mx = fmaxf(mx, sc[k]);
+      }
+      // block max of each head: lanes of the head within the token set, then across token sets
+#pragma unroll
+      for (int m = 1; m < Gm::HEAD_LANES; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+#pragma unroll
+      for (int m = Gm::CPR; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+      float m_mine = 0.f, alpha_mine = 1.f;
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+        const float mb = __shfl_sync(0xffffffffu, mx, hh * Gm::HEAD_LANES);
+        // lazy rescale: move the reference max only when the block exceeds it by a margin
+        if (mb > m_run[hh] + kLazyRescale || (m_run[hh] == -INFINITY && mb != -INFINITY)) {
+          const float alpha = fast_exp2(m_run[hh] - mb);  // 0 when m_run was -inf
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[hh][e] *= alpha;
+          if (hh == my_head) alpha_mine = alpha;
+          m_run[hh] = mb;
+        }
+        if (hh == my_head) m_mine = m_run[hh];
+      }
+      l_part *= alpha_mine;
+      float pk[Gm::R];
+#pragma unroll
+      for (int k = 0; k < Gm::R; ++k) {
+        pk[k] = (sc[k] == -INFINITY) ? 0.f : fast_exp2(sc[k] - m_mine);
+        if (counts_sum) l_part += pk[k];
+      }
+      // every lane needs p of its own tokens for all heads
+      float pv[G][Gm::TPL];
+#pragma unroll
+      for (int hh = 0; hh < G; ++hh) {
+#pragma unroll
+        for (int i2 = 0; i2 < Gm::TPL; ++i2) {
+          const int idx = hh * Gm::TPL + i2;
+          const int src = ts * Gm::CPR + (idx / Gm::R) * Gm::SHARE;
+          pv[hh][i2] = __shfl_sync(0xffffffffu, pk[idx % Gm::R], src);
+        }
+      }
+#pragma unroll
+      for (int i2 = 0; i2 < Gm::TPL; ++i2) {
+        const int t = Gm::TS * i2 + ts;
+        if (tok0 + t >= t_end) continue;  // slots past the context may hold anything (even NaN)
+        const uint4 vw = *reinterpret_cast<const uint4*>(vb + t * (D * 2) + cl * 16);
+        const float vf[8] = {bf16lo_to_f32(vw.x), bf16hi_to_f32(vw.x), bf16lo_to_f32(vw.y), bf16hi_to_f32(vw.y),
+                             bf16lo_to_f32(vw.z), bf16hi_to_f32(vw.z), bf16lo_to_f32(vw.w), bf16hi_to_f32(vw.w)};
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) o[hh][e] = fmaf(pv[hh][i2], vf[e], o[hh][e]);
+        }
+      }
+    }
+    __syncwarp();
+    if (i + kStages < my_n) {
+      const int nb = __shfl_sync(0xffffffffu, my_blk, i + kStages);
+      if (lane == 0) issue(i + kStages, nb);
+      issued = i + kStages + 1;
+    }
+  }
+  if (!ok) {
+    // let copies still in flight land before the shared memory is released
+    for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
+      drain_wait(&wbar[i % kStages], (i / kStages) & 1);
+  }
+
+  // ---- warp totals: sum over the lanes of a head, and over token sets
+#pragma unroll
+  for (int m = 1; m < Gm::HEAD_LANES; m <<= 1) l_part += __shfl_xor_sync(0xffffffffu, l_part, m);
+#pragma unroll
+  for (int m = Gm::CPR; m < 32; m <<= 1) l_part += __shfl_xor_sync(0xffffffffu, l_part, m);
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+#pragma unroll
+      for (int m = Gm::CPR; m < 32; m <<= 1) o[hh][e] += __shfl_xor_sync(0xffffffffu, o[hh][e], m);
+    }
+  }
+  constexpr int kRec = D + 2;  // per (warp, head): o[D], m, l
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh) {
+    const float lh = __shfl_sync(0xffffffffu, l_part, hh * Gm::HEAD_LANES);
+    float* rec = comb + (warp * G + hh) * kRec;
+    if (ts == 0) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) rec[cl * 8 + e] = o[hh][e];
+    }
+    if (lane == 0) {
+      rec[D] = ok ? m_run[hh] : -INFINITY;
+      rec[D + 1] = ok ? lh : 0.f;
+    }
+  }
+  __syncthreads();
+
+  // ---- combine the warps and write this split's partial (normalised out, log2 LSE)
+  for (int x = threadIdx.x; x < G * D; x += kWarps * 32) {
+    const int hh = x / D, d = x % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, comb[(w * G + hh) * kRec + D]);
+    float lsum = 0.f, osum = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float* rec = comb + (w * G + hh) * kRec;
+        if (rec[D] == -INFINITY) continue;
+        const float sc = fast_exp2(rec[D] - M);
+        lsum = fmaf(sc, rec[D + 1], lsum);
+        osum = fmaf(sc, rec[d], osum);
+      }
+    }
+    const int h = g * G + hh;
+    const int64_t slot = (static_cast<int64_t>(b) * p.Hq + h) * p.n_split + split;
+    const bool empty = !(lsum > 0.f);
+    p.o_part[slot * D + d] = empty ? 0.f : osum / lsum;
+    if (d == 0) p.lse_part[slot] = empty ? -INFINITY : M + __log2f(lsum);
+  }
+}
+
+// Merge the splits of each (sequence, head): the LSE rule of the ring-attention
+// page, with the LSEs in log2 units.  One warp per (sequence, head).
+template <int D>
+__global__ void decode_reduce_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+                                     const int32_t* __restrict__ ctx_lens, int max_tokens, int n_split,
+                                     int64_t B, int Hq, void* out, int out_bf16, int64_t os0, int64_t os1,
+                                     float* lse) {
+  constexpr int DPL = D / 32;  // dims per lane
+  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= B * Hq) return;
+  const int64_t b = wid / Hq;
+  const int h = static_cast<int>(wid % Hq);
+  int L = ctx_lens[b];
+  L = L < 0 ? 0 : (L > max_tokens ? max_tokens : L);
+  const int ns = (L + kDecodeSplitTokens - 1) / kDecodeSplitTokens;
+  const int64_t base = wid * n_split;
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) M = fmaxf(M, lse_part[base + s]);
+  float acc[DPL];
+#pragma unroll
+  for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+  float wsum = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < ns; ++s) {
+      const float ls = lse_part[base + s];
+      if (ls == -INFINITY) continue;
+      const float w = fast_exp2(ls - M);
+      wsum += w;
+      const float* op = o_part + (base + s) * D + lane * DPL;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) acc[e] = fmaf(w, op[e], acc[e]);
+    }
+  }
+  const bool empty = !(wsum > 0.f);
+  const float inv = empty ? 0.f : 1.f / wsum;
+  const int64_t ob = b * os0 + h * os1 + lane * DPL;
+  if (out_bf16) {
+    uint16_t* dst = static_cast<uint16_t*>(out) + ob;
+#pragma unroll
+    for (int e = 0; e < DPL; e += 2)
+      *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+  } else {
+    float* dst = static_cast<float*>(out) + ob;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) dst[e] = acc[e] * inv;
+  }
+  if (lse != nullptr && lane == 0)
+    lse[wid] = empty ? -INFINITY : (M + __log2f(wsum)) * 0.6931471805599453f;
+}
+
+template <int D, int G>
+cudaError_t launch_decode(const DecodeArgs& a, const DecodeParams& p, cudaStream_t stream) {
+  using Gm = Geo<D, G>;
+  const int smem = kWarps * kStages * 2 * Gm::BLOCK_BYTES + kWarps * kStages * 8 + kWarps * G * (D + 2) * 4;
+  auto kern = paged_decode_kernel<D, G>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(static_cast<unsigned>(a.n_split), static_cast<unsigned>(a.cache.Hkv), static_cast<unsigned>(a.B));
+  kern<<<grid, kWarps * 32, smem, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t warps = a.B * a.Hq;
+  const unsigned blocks = static_cast<unsigned>((warps * 32 + 127) / 128);
+  decode_reduce_kernel<D><<<blocks, 128, 0, stream>>>(p.o_part, p.lse_part, a.ctx_lens, a.max_blocks * kBS,
+                                                     a.n_split, a.B, static_cast<int>(a.Hq), a.out.data,
+                                                     a.out.dtype == ATTN_BF16, a.out.stride[0], a.out.stride[1],
+                                                     a.lse);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_decode_d(const DecodeArgs& a, const DecodeParams& p, cudaStream_t stream) {
+  switch (a.Hq / a.cache.Hkv) {
+    case 1: return launch_decode<D, 1>(a, p, stream);
+    case 2: return launch_decode<D, 2>(a, p, stream);
+    case 4: return launch_decode<D, 4>(a, p, stream);
+    case 8: return launch_decode<D, 8>(a, p, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
+  DecodeParams p;
+  p.kc = static_cast<const uint16_t*>(a.cache.k);
+  p.vc = static_cast<const uint16_t*>(a.cache.v);
+  p.num_blocks = a.cache.num_blocks;
+  p.Hkv = a.cache.Hkv;
+  p.q = static_cast<const uint16_t*>(a.q.data);
+  p.q_stride[0] = a.q.stride[0];
+  p.q_stride[1] = a.q.stride[1];
+  p.bt = a.block_table;
+  p.bt_stride = a.bt_stride;
+  p.max_blocks = a.max_blocks;
+  p.ctx_lens = a.ctx_lens;
+  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  const size_t n = static_cast<size_t>(a.B) * a.Hq * a.n_split;
+  p.o_part = static_cast<float*>(a.partials);
+  p.lse_part = p.o_part + n * a.cache.D;
+  p.n_split = a.n_split;
+  p.Hq = static_cast<int>(a.Hq);
+  p.status = a.status;
+  if (a.cache.D == 64) return launch_decode_d<64>(a, p, stream);
+  if (a.cache.D == 128) return launch_decode_d<128>(a, p, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

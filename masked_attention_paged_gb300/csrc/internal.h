@@ -1,0 +1,102 @@
+// internal.h -- host-side interface between the C ABI (api.cu) and the
+// kernel launchers.  Arguments reaching these functions are validated.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "libattn.h"
+
+namespace attn {
+
+struct View4 {
+  void* data;
+  int dtype;  // attn_dtype
+  int64_t shape[4];
+  int64_t stride[4];  // elements
+};
+
+struct AttnFwdArgs {
+  int64_t B, Hq, Hkv, Pq, Pk, D;
+  View4 q, k, v, out;
+  const float* mask;  // [B, Pk] additive, row stride mask_stride; may be null
+  int64_t mask_stride;
+  float scale;
+  float* lse;         // [B, Hq, Pq] contiguous, may be null
+  uint32_t* status;   // device status word
+};
+
+// bf16 inputs, D in {64, 128}: tcgen05 + TMA kernel
+cudaError_t launch_attn_fwd_tc(const AttnFwdArgs& a, cudaStream_t stream);
+// f32 inputs, D <= 128, D % 4 == 0: FFMA kernel
+cudaError_t launch_attn_fwd_simt(const AttnFwdArgs& a, cudaStream_t stream);
+// Pk == 0: out = 0, lse = -inf
+cudaError_t launch_attn_empty_keys(const AttnFwdArgs& a, cudaStream_t stream);
+
+struct MergeArgs {
+  int n;
+  int64_t B, H, P, D;
+  View4 outs[8];
+  const float* lses[8];
+  View4 out;
+  float* lse;
+};
+cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t stream);
+
+struct PagedCache {
+  void* k;
+  void* v;
+  int64_t num_blocks;
+  int block_size;
+  int Hkv;
+  int D;
+};
+
+struct AppendArgs {
+  PagedCache cache;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int max_blocks;
+  const int32_t* pos;
+  int64_t B;
+  View4 k_new, v_new;  // [B, Hkv, D] (shape[3] unused)
+  uint32_t* status;
+};
+cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
+
+struct GatherArgs {
+  PagedCache cache;
+  int which;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int max_blocks;
+  const int32_t* lens;
+  int64_t B;
+  int64_t max_len;
+  void* dst;
+  uint32_t* status;
+};
+cudaError_t launch_paged_gather(const GatherArgs& a, cudaStream_t stream);
+
+struct DecodeArgs {
+  PagedCache cache;
+  View4 q;    // [B, Hq, D]
+  View4 out;  // [B, Hq, D]
+  float* lse; // [B, Hq] or null
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int max_blocks;
+  const int32_t* ctx_lens;
+  int64_t B, Hq;
+  float scale;
+  void* partials;  // workspace after the status block
+  int n_split;     // split slots per (sequence, head) in the partial buffer
+  uint32_t* status;
+};
+// tokens per split-K work unit of the paged decode
+constexpr int kDecodeSplitTokens = 512;
+int decode_num_splits(int max_blocks, int block_size);
+size_t decode_partial_bytes(int64_t B, int64_t Hq, int n_split, int D);
+cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);
+
+}  // namespace attn

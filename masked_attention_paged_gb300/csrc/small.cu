@@ -1,0 +1,291 @@
+// small.cu -- the bandwidth-bound kernels around the attention kernels:
+//   kv_append       one token's K/V per sequence into the paged cache
+//   paged_gather    paged cache -> contiguous copy (test/debug export)
+//   lse_merge       n-way merge of chunk results through their LSE
+//   empty_keys      out = 0, lse = -inf when there are no keys at all
+// All moves are 16-byte vectors; append and gather are bit copies.
+#include <math.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace attn {
+namespace {
+
+// ---------------------------------------------------------------------------
+// kv_append ("KV cache in nanoVLM": the decode step computes K/V of the newest
+// token only and adds it to the cache).  One CTA per sequence; each thread
+// moves 16 bytes of K and 16 bytes of V.
+// ---------------------------------------------------------------------------
+struct AppendParams {
+  uint16_t* kc;
+  uint16_t* vc;
+  int64_t num_blocks;
+  int block_size, Hkv, D;
+  const int32_t* bt;
+  int64_t bt_stride;
+  int max_blocks;
+  const int32_t* pos;
+  const uint16_t* kn;
+  const uint16_t* vn;
+  int64_t kn_stride[2], vn_stride[2];  // batch, head (elements)
+  uint32_t* status;
+};
+
+__global__ void kv_append_kernel(const AppendParams p) {
+  const int b = blockIdx.x;
+  const int pos = p.pos[b];
+  if (pos < 0) return;  // idle sequence
+  const int lb = pos / p.block_size;
+  if (lb >= p.max_blocks) {
+    if (threadIdx.x == 0) report(p.status, kStatusBounds);
+    return;
+  }
+  const int blk = p.bt[static_cast<int64_t>(b) * p.bt_stride + lb];
+  if (blk < 0 || blk >= p.num_blocks) {
+    if (threadIdx.x == 0) report(p.status, kStatusBounds);
+    return;
+  }
+  const int slot = pos % p.block_size;
+  const int vec_per_head = p.D / 8;
+  for (int i = threadIdx.x; i < p.Hkv * vec_per_head; i += blockDim.x) {
+    const int g = i / vec_per_head;
+    const int c = (i % vec_per_head) * 8;
+    const int64_t dst = ((static_cast<int64_t>(blk) * p.Hkv + g) * p.block_size + slot) * p.D + c;
+    const uint4 kv = *reinterpret_cast<const uint4*>(p.kn + b * p.kn_stride[0] + g * p.kn_stride[1] + c);
+    const uint4 vv = *reinterpret_cast<const uint4*>(p.vn + b * p.vn_stride[0] + g * p.vn_stride[1] + c);
+    *reinterpret_cast<uint4*>(p.kc + dst) = kv;
+    *reinterpret_cast<uint4*>(p.vc + dst) = vv;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// paged_gather: dst[b, g, t, :] = cache[block_table[b][t / bs], g, t % bs, :]
+// grid (token tiles of 16, Hkv, B); 16-byte vectors.
+// ---------------------------------------------------------------------------
+struct GatherParams {
+  const uint16_t* cache;
+  int64_t num_blocks;
+  int block_size, Hkv, D;
+  const int32_t* bt;
+  int64_t bt_stride;
+  int max_blocks;
+  const int32_t* lens;
+  int64_t max_len;
+  uint16_t* dst;
+  uint32_t* status;
+};
+
+__global__ void paged_gather_kernel(const GatherParams p) {
+  const int b = blockIdx.z, g = blockIdx.y;
+  const int L = p.lens[b];
+  const int vec = p.D / 8;
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * 16;
+  for (int i = threadIdx.x; i < 16 * vec; i += blockDim.x) {
+    const int64_t t = t0 + i / vec;
+    if (t >= L || t >= p.max_len) continue;
+    const int64_t lb = t / p.block_size;
+    if (lb >= p.max_blocks) {
+      report(p.status, kStatusBounds);
+      continue;
+    }
+    const int blk = p.bt[static_cast<int64_t>(b) * p.bt_stride + lb];
+    if (blk < 0 || blk >= p.num_blocks) {
+      report(p.status, kStatusBounds);
+      continue;
+    }
+    const int c = (i % vec) * 8;
+    const int64_t src = ((static_cast<int64_t>(blk) * p.Hkv + g) * p.block_size + t % p.block_size) * p.D + c;
+    const int64_t dst = ((static_cast<int64_t>(b) * p.Hkv + g) * p.max_len + t) * p.D + c;
+    *reinterpret_cast<uint4*>(p.dst + dst) = *reinterpret_cast<const uint4*>(p.cache + src);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// lse_merge ("[sglang] ROCm aiter ring attention", section 1):
+//   lse = M + log(sum_i exp(lse_i - M)),  out = sum_i exp(lse_i - lse) out_i
+// Each group of D/8 threads owns one (b, h, p) row; rows are walked in the
+// order of the contiguous LSE layout so the LSE reads coalesce.
+// ---------------------------------------------------------------------------
+struct MergeParams {
+  int n;
+  int64_t H, P, D, rows;
+  const void* outs[8];
+  int64_t ostride[8][3];
+  const float* lses[8];
+  int in_bf16;
+  void* out;
+  int64_t out_stride[3];
+  int out_bf16;
+  float* lse;
+};
+
+__device__ __forceinline__ void load8(const void* base, int64_t off, bool bf16, float (&v)[8]) {
+  if (bf16) {
+    const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + off);
+    v[0] = bf16lo_to_f32(w.x); v[1] = bf16hi_to_f32(w.x);
+    v[2] = bf16lo_to_f32(w.y); v[3] = bf16hi_to_f32(w.y);
+    v[4] = bf16lo_to_f32(w.z); v[5] = bf16hi_to_f32(w.z);
+    v[6] = bf16lo_to_f32(w.w); v[7] = bf16hi_to_f32(w.w);
+  } else {
+    const float4* f = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
+    const float4 a = f[0], c = f[1];
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+  }
+}
+
+__global__ void lse_merge_kernel(const MergeParams p) {
+  const int vec = static_cast<int>(p.D / 8);
+  const int64_t total = p.rows * vec;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = idx / vec;
+    const int c = static_cast<int>(idx % vec) * 8;
+    const int64_t pp = r % p.P, hh = (r / p.P) % p.H, bb = r / (p.P * p.H);
+    float l[8];
+    float M = -INFINITY;
+    for (int i = 0; i < p.n; ++i) {
+      l[i] = p.lses[i][r];
+      M = fmaxf(M, l[i]);
+    }
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float lse = -INFINITY;
+    if (M != -INFINITY) {
+      float tot = 0.f;
+      for (int i = 0; i < p.n; ++i) tot += expf(l[i] - M);
+      lse = M + logf(tot);
+      for (int i = 0; i < p.n; ++i) {
+        const float w = expf(l[i] - lse);
+        if (w == 0.f) continue;
+        float v[8];
+        load8(p.outs[i], bb * p.ostride[i][0] + hh * p.ostride[i][1] + pp * p.ostride[i][2] + c, p.in_bf16, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(w, v[e], acc[e]);
+      }
+    }
+    const int64_t o = bb * p.out_stride[0] + hh * p.out_stride[1] + pp * p.out_stride[2] + c;
+    if (p.out_bf16) {
+      uint4 w;
+      w.x = pack_bf16x2(acc[0], acc[1]);
+      w.y = pack_bf16x2(acc[2], acc[3]);
+      w.z = pack_bf16x2(acc[4], acc[5]);
+      w.w = pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + o) = w;
+    } else {
+      float4* f = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o);
+      f[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      f[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+    if (p.lse != nullptr && c == 0) p.lse[r] = lse;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// no keys: out = 0, lse = -inf
+// ---------------------------------------------------------------------------
+__global__ void empty_keys_kernel(void* out, int out_bf16, int64_t s0, int64_t s1, int64_t s2, int64_t H,
+                                  int64_t P, int64_t D, float* lse) {
+  const int64_t r = blockIdx.x;  // (b * H + h) * P + p
+  const int64_t pp = r % P, hh = (r / P) % H, bb = r / (P * H);
+  const int64_t o = bb * s0 + hh * s1 + pp * s2;
+  for (int64_t d = threadIdx.x; d < D; d += blockDim.x) {
+    if (out_bf16)
+      static_cast<uint16_t*>(out)[o + d] = 0;
+    else
+      static_cast<float*>(out)[o + d] = 0.f;
+  }
+  if (lse != nullptr && threadIdx.x == 0) lse[r] = -INFINITY;
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
+  AppendParams p;
+  p.kc = static_cast<uint16_t*>(a.cache.k);
+  p.vc = static_cast<uint16_t*>(a.cache.v);
+  p.num_blocks = a.cache.num_blocks;
+  p.block_size = a.cache.block_size;
+  p.Hkv = a.cache.Hkv;
+  p.D = a.cache.D;
+  p.bt = a.block_table;
+  p.bt_stride = a.bt_stride;
+  p.max_blocks = a.max_blocks;
+  p.pos = a.pos;
+  p.kn = static_cast<const uint16_t*>(a.k_new.data);
+  p.vn = static_cast<const uint16_t*>(a.v_new.data);
+  p.kn_stride[0] = a.k_new.stride[0];
+  p.kn_stride[1] = a.k_new.stride[1];
+  p.vn_stride[0] = a.v_new.stride[0];
+  p.vn_stride[1] = a.v_new.stride[1];
+  p.status = a.status;
+  const int threads = std::min(256, std::max(32, a.cache.Hkv * a.cache.D / 8));
+  kv_append_kernel<<<static_cast<unsigned>(a.B), threads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_paged_gather(const GatherArgs& a, cudaStream_t stream) {
+  GatherParams p;
+  p.cache = static_cast<const uint16_t*>(a.which ? a.cache.v : a.cache.k);
+  p.num_blocks = a.cache.num_blocks;
+  p.block_size = a.cache.block_size;
+  p.Hkv = a.cache.Hkv;
+  p.D = a.cache.D;
+  p.bt = a.block_table;
+  p.bt_stride = a.bt_stride;
+  p.max_blocks = a.max_blocks;
+  p.lens = a.lens;
+  p.max_len = a.max_len;
+  p.dst = static_cast<uint16_t*>(a.dst);
+  p.status = a.status;
+  dim3 grid(static_cast<unsigned>((a.max_len + 15) / 16), static_cast<unsigned>(a.cache.Hkv),
+            static_cast<unsigned>(a.B));
+  paged_gather_kernel<<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t stream) {
+  MergeParams p;
+  p.n = a.n;
+  p.H = a.H;
+  p.P = a.P;
+  p.D = a.D;
+  p.rows = a.B * a.H * a.P;
+  for (int i = 0; i < a.n; ++i) {
+    p.outs[i] = a.outs[i].data;
+    p.ostride[i][0] = a.outs[i].stride[0];
+    p.ostride[i][1] = a.outs[i].stride[1];
+    p.ostride[i][2] = a.outs[i].stride[2];
+    p.lses[i] = a.lses[i];
+  }
+  p.in_bf16 = a.outs[0].dtype == ATTN_BF16;
+  p.out = a.out.data;
+  p.out_stride[0] = a.out.stride[0];
+  p.out_stride[1] = a.out.stride[1];
+  p.out_stride[2] = a.out.stride[2];
+  p.out_bf16 = a.out.dtype == ATTN_BF16;
+  p.lse = a.lse;
+  const int64_t threads_total = p.rows * (a.D / 8);
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t want = (threads_total + 255) / 256;
+  const int64_t cap = static_cast<int64_t>(sms) * 16;
+  const unsigned blocks = static_cast<unsigned>(std::max<int64_t>(1, std::min(want, cap)));
+  lse_merge_kernel<<<blocks, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_empty_keys(const AttnFwdArgs& a, cudaStream_t stream) {
+  const int64_t rows = a.B * a.Hq * a.Pq;
+  if (rows == 0) return cudaSuccess;
+  if (rows > 0x7fffffffLL) return cudaErrorInvalidValue;
+  empty_keys_kernel<<<static_cast<unsigned>(rows), 64, 0, stream>>>(
+      a.out.data, a.out.dtype == ATTN_BF16, a.out.stride[0], a.out.stride[1], a.out.stride[2], a.Hq, a.Pq, a.D,
+      a.lse);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

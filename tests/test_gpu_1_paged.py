@@ -1,0 +1,180 @@
+"""GPU parity of the paged-cache calls against the oracle: kv_append and the
+block-table gather bit for bit, paged GQA decode within the bf16 tolerances,
+at small ragged sizes and at the full decode workload (64 sequences, 32 query
+heads over 8 KV heads, D 128, contexts uniform in [512, 8192])."""
+import numpy as np
+import pytest
+import torch
+
+import masked_attention_paged_gb300 as lib
+import oracle
+import workloads
+from _parity import assert_lse_close, assert_out_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _dev(d: workloads.DecodeInputs):
+    return {k: getattr(d, k).to(DEV) for k in ("k_cache", "v_cache", "block_table", "pos", "ctx_lens", "ctx",
+                                               "k_new", "v_new", "q")}
+
+
+SMALL = workloads.DecodeConfig("small", 7, 8, 2, 128, 16, 0, 1100, 5)
+
+
+@pytest.mark.parametrize("D,ctx", [(128, [0, 1, 15, 16, 17, 511, 512]), (64, [3, 31, 32, 33, 700, 1023, 1100])])
+def test_kv_append_bit_exact(D, ctx):
+    cfg = workloads.DecodeConfig("a", len(ctx), 8, 2, D, 16, 0, 1100, 5)
+    d = workloads.make_decode_inputs(cfg, seed=3, ctx=ctx)
+    g = _dev(d)
+    ws = lib.Workspace(256)
+    lib.kv_append(g["k_cache"], g["v_cache"], g["block_table"], g["pos"], g["k_new"], g["v_new"], workspace=ws)
+    ek, ev = oracle.kv_append(d.k_cache, d.v_cache, d.block_table, d.pos, d.k_new, d.v_new)
+    # NaN sentinels compare as bits, so untouched slots must keep their exact pattern
+    assert np.array_equal(g["k_cache"].cpu().view(torch.int16).numpy(), ek)
+    assert np.array_equal(g["v_cache"].cpu().view(torch.int16).numpy(), ev)
+    assert ws.status() == 0
+
+
+def test_kv_append_skips_idle_and_flags_bad_positions():
+    d = workloads.make_decode_inputs(SMALL, seed=4, ctx=[5, 6, 7, 8, 9, 10, 11])
+    g = _dev(d)
+    pos = g["pos"].clone()
+    pos[1] = -1  # idle sequence: nothing written
+    pos[2] = 16 * d.block_table.shape[1]  # past the table
+    ws = lib.Workspace(256)
+    before = g["k_cache"].clone()
+    lib.kv_append(g["k_cache"], g["v_cache"], g["block_table"], pos, g["k_new"], g["v_new"], workspace=ws)
+    assert ws.status() == 5  # ATTN_ERR_DEVICE_BOUNDS
+    p2 = pos.cpu().clone()
+    p2[1] = d.pos[1]
+    p2[2] = d.pos[2]
+    exp_k, _ = oracle.kv_append(d.k_cache, d.v_cache, d.block_table, d.pos, d.k_new, d.v_new)
+    got = g["k_cache"].cpu().view(torch.int16).numpy()
+    for b in range(7):
+        blk = int(d.block_table[b, int(d.pos[b]) // 16])
+        slot = int(d.pos[b]) % 16
+        if b in (1, 2):
+            assert np.array_equal(got[blk, :, slot], before.cpu().view(torch.int16).numpy()[blk, :, slot])
+        else:
+            assert np.array_equal(got[blk, :, slot], exp_k[blk, :, slot])
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_paged_gather_bit_exact(D):
+    cfg = workloads.DecodeConfig("g", 5, 8, 4, D, 16, 1, 900, 3)
+    d = workloads.make_decode_inputs(cfg, seed=5, ctx=[1, 16, 17, 512, 900])
+    g = _dev(d)
+    max_len = int(d.ctx.max())
+    got = lib.paged_kv_gather(g["k_cache"], g["block_table"], g["ctx"], max_len)
+    exp = oracle.paged_gather(d.k_cache, d.block_table, d.ctx)
+    got_bits = got.cpu().view(torch.int16).numpy()
+    for b in range(5):
+        L = int(d.ctx[b])
+        assert np.array_equal(got_bits[b, :, :L], exp[b])
+        assert np.all(got_bits[b, :, L:] == 0)
+
+
+def test_gather_flags_bad_block_ids():
+    d = workloads.make_decode_inputs(SMALL, seed=6, ctx=[40] * 7)
+    g = _dev(d)
+    bt = g["block_table"].clone()
+    bt[3, 1] = d.num_blocks + 5
+    ws = lib.Workspace(256)
+    lib.paged_kv_gather(g["k_cache"], bt, g["ctx"], 40, workspace=ws)
+    assert ws.status() == 5
+
+
+def _decode_and_check(d: workloads.DecodeInputs, seed_note=""):
+    g = _dev(d)
+    ws = lib.Workspace(lib.paged_decode_workspace_size(d.cfg.B, d.cfg.Hq, d.block_table.shape[1], 16, d.cfg.D))
+    lib.kv_append(g["k_cache"], g["v_cache"], g["block_table"], g["pos"], g["k_new"], g["v_new"], workspace=ws)
+    out, lse = lib.paged_decode_attn(g["q"], g["k_cache"], g["v_cache"], g["block_table"], g["ctx_lens"], d.scale,
+                                     return_lse=True, workspace=ws)
+    assert ws.status() == 0
+    ek, ev = oracle.kv_append(d.k_cache, d.v_cache, d.block_table, d.pos, d.k_new, d.v_new)
+    ro, rl = oracle.paged_decode(d.q, torch.from_numpy(ek).view(torch.bfloat16),
+                                 torch.from_numpy(ev).view(torch.bfloat16), d.block_table, d.ctx_lens, d.scale)
+    assert_out_close(out, ro, what="decode out" + seed_note)
+    assert_lse_close(lse, rl, what="decode lse" + seed_note)
+    return out
+
+
+@pytest.mark.parametrize("D,G", [(128, 4), (128, 1), (128, 8), (64, 4), (64, 2)])
+def test_paged_decode_small(D, G):
+    Hkv = 2
+    cfg = workloads.DecodeConfig("s", 9, G * Hkv, Hkv, D, 16, 0, 1500, 4)
+    # L = ctx + 1: 1 token, a full block, one past a block, a whole split, one
+    # past a split, several splits with a ragged tail
+    d = workloads.make_decode_inputs(cfg, seed=7, ctx=[0, 15, 16, 511, 512, 1023, 1024, 1300, 1500])
+    _decode_and_check(d, f" D={D} G={G}")
+
+
+def test_paged_decode_f32_output_and_strided_q():
+    cfg = workloads.DecodeConfig("s", 3, 8, 2, 128, 16, 100, 600, 2)
+    d = workloads.make_decode_inputs(cfg, seed=8)
+    g = _dev(d)
+    lib.kv_append(g["k_cache"], g["v_cache"], g["block_table"], g["pos"], g["k_new"], g["v_new"])
+    # q as a strided view (heads of a wider buffer)
+    qbuf = torch.zeros(3, 16, 128, dtype=torch.bfloat16, device=DEV)
+    qbuf[:, ::2] = g["q"]
+    qv = qbuf[:, ::2]
+    out = torch.empty(3, 8, 128, dtype=torch.float32, device=DEV)
+    lib.paged_decode_attn(qv, g["k_cache"], g["v_cache"], g["block_table"], g["ctx_lens"], d.scale, out=out)
+    ek, ev = oracle.kv_append(d.k_cache, d.v_cache, d.block_table, d.pos, d.k_new, d.v_new)
+    ro, _ = oracle.paged_decode(d.q, torch.from_numpy(ek).view(torch.bfloat16),
+                                torch.from_numpy(ev).view(torch.bfloat16), d.block_table, d.ctx_lens, d.scale)
+    assert_out_close(out, ro, what="decode f32 out")
+
+
+def test_paged_decode_empty_context_and_bad_block():
+    cfg = workloads.DecodeConfig("e", 3, 8, 2, 128, 16, 0, 200, 2)
+    d = workloads.make_decode_inputs(cfg, seed=9, ctx=[10, 100, 200])
+    g = _dev(d)
+    lens = g["ctx"].clone()
+    lens[0] = 0  # no tokens at all
+    ws = lib.Workspace(lib.paged_decode_workspace_size(3, 8, d.block_table.shape[1], 16, 128))
+    out, lse = lib.paged_decode_attn(g["q"], g["k_cache"], g["v_cache"], g["block_table"], lens, d.scale,
+                                     return_lse=True, workspace=ws)
+    assert ws.status() == 0
+    assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
+    lens_cpu = lens.cpu()
+    ro, rl = oracle.paged_decode(d.q[1:], d.k_cache, d.v_cache, d.block_table[1:], lens_cpu[1:], d.scale)
+    assert_out_close(out[1:], ro)
+    assert_lse_close(lse[1:], rl)
+    # a table entry outside the cache is reported, and the call neither faults nor hangs
+    bt = g["block_table"].clone()
+    bt[2, 3] = -7
+    ws.reset()
+    lib.paged_decode_attn(g["q"], g["k_cache"], g["v_cache"], bt, lens, d.scale, workspace=ws)
+    assert ws.status() == 5
+
+
+def test_paged_decode_full_workload():
+    """64 sequences x 32 query heads, KV heads 8, D 128, contexts U[512, 8192]:
+    append then decode, every output against the oracle."""
+    d = workloads.make_decode_inputs(workloads.DECODE_CONFIGS["decode"], seed=0)
+    _decode_and_check(d, " full")
+
+
+def test_incremental_decode_equals_recompute_on_gpu():
+    """The decode of the appended token equals the last row of full attention
+    over the gathered contiguous sequence, both computed on the GPU
+    (paged_decode_attn vs attn_fwd over paged_kv_gather output)."""
+    cfg = workloads.DecodeConfig("r", 4, 8, 2, 128, 16, 300, 900, 2)
+    d = workloads.make_decode_inputs(cfg, seed=10)
+    g = _dev(d)
+    lib.kv_append(g["k_cache"], g["v_cache"], g["block_table"], g["pos"], g["k_new"], g["v_new"])
+    out, lse = lib.paged_decode_attn(g["q"], g["k_cache"], g["v_cache"], g["block_table"], g["ctx_lens"], d.scale,
+                                     return_lse=True)
+    Lmax = int(d.ctx_lens.max())
+    kcont = lib.paged_kv_gather(g["k_cache"], g["block_table"], g["ctx_lens"], Lmax)
+    vcont = lib.paged_kv_gather(g["v_cache"], g["block_table"], g["ctx_lens"], Lmax)
+    for b in range(4):
+        L = int(d.ctx_lens[b])
+        o2, l2 = lib.attn_fwd(g["q"][b:b + 1].unsqueeze(2).contiguous(), kcont[b:b + 1, :, :L].contiguous(),
+                              vcont[b:b + 1, :, :L].contiguous(), None, d.scale)
+        diff = (o2[0, :, 0].float() - out[b].float()).abs().max().item()
+        assert diff <= 2e-2
+        assert (l2[0, :, 0] - lse[b]).abs().max().item() <= 1e-3
