@@ -201,5 +201,6 @@ def test_no_score_matrix_is_allocated():
     Ps = np.array(sorted(extra), dtype=float)
     ys = np.array([extra[int(p)] for p in Ps], dtype=float)
     quad = np.polyfit(Ps, ys, 2)[0]
-    # a P^2 term of even 1/1000 of one bf16 score matrix per head would be 0.032 B/P^2
-    assert abs(quad) < 1e-3, quad
+    # one bf16 score matrix of 16 heads is 32 B per P^2; the fit (whose noise is the
+    # allocator's 2 MB rounding, about 0.02 B/P^2 here) must stay under 1% of that
+    assert abs(quad) < 0.01 * 16 * 2, quad
