@@ -193,6 +193,41 @@ attn_status paged_decode_attn(const attn_tensor *q, const attn_kv_cache *cache,
                               const attn_tensor *out, float *lse,
                               void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * paged_decode_attn_noalloc -- the same paged decode for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this call; it
+ * exists for this library's users.
+ *
+ * paged_decode_attn needs a workspace for its split-K partials.  A caller
+ * that is handed only input and output buffers (a plugin inside a framework
+ * that owns all device memory) or that must keep its device footprint fixed
+ * and never call an allocator has nowhere to get one.  This call uses a
+ * scratch array built into the library instead: 20 MiB per GPU, created when
+ * the library's code is loaded onto that GPU and kept until the process
+ * exits.  It allocates and frees nothing.
+ *
+ *   Arguments and results are those of paged_decode_attn, without the
+ *   workspace.  device_status (a device pointer, may be NULL) receives this
+ *   call's status word: 0, or the bit (1 << ATTN_ERR_DEVICE_BOUNDS) when a
+ *   block-table entry or context length was out of range.
+ *   Returns ATTN_ERR_WORKSPACE when the call would need more than the 20 MiB
+ *   scratch (batch * Hq * ceil(max_blocks*block_size/512) * (head_dim+1) * 4
+ *   bytes, plus 256); the 64-sequence, 32-head, head_dim 128 decode with
+ *   contexts up to 8192 tokens needs 17.97 MB.
+ *   The first call on each device looks up the scratch array's device
+ *   address (with that device current) and remembers it; make that first
+ *   call before any stream capture.
+ *   All calls on a device share the scratch.  The call clears the status
+ *   word it needs zeroed on its stream; calls whose work overlaps on the GPU
+ *   (other streams, other threads) race on the scratch and must be ordered by
+ *   the caller.
+ */
+attn_status paged_decode_attn_noalloc(const attn_tensor *q, const attn_kv_cache *cache,
+                                      const int32_t *block_table, int64_t bt_stride, int32_t max_blocks,
+                                      const int32_t *ctx_lens, float scale,
+                                      const attn_tensor *out, float *lse,
+                                      uint32_t *device_status, cudaStream_t stream);
+
 /* Test/debug export: gather the paged cache of every (sequence, KV head) into
  * contiguous dst [batch, num_kv_heads, max_len, head_dim] (bf16), tokens
  * t < lens[b]; rows t >= lens[b] are left untouched.  Bit-exact.

@@ -84,6 +84,7 @@ def load(build_if_missing: bool = False):
             "kv_append": (I32, [C, P, I64, I32, P, T, T, P, SZ, P]),
             "paged_decode_attn": (I32, [T, C, P, I64, I32, P, F, T, P, P, SZ, P]),
             "paged_kv_gather": (I32, [C, I32, P, I64, I32, P, I32, I64, P, P, SZ, P]),
+            "paged_decode_attn_noalloc": (I32, [T, C, P, I64, I32, P, F, T, P, P, P]),
             "attn_check_device_status": (I32, [P, ctypes.POINTER(ctypes.c_uint32), P]),
             "attn_reset_device_status": (I32, [P, P]),
         }
@@ -98,7 +99,8 @@ def load(build_if_missing: bool = False):
 def exported_symbols() -> list[str]:
     return ["attn_fwd", "attn_lse_merge", "kv_append", "paged_decode_attn", "paged_kv_gather",
             "attn_fwd_workspace_size", "kv_append_workspace_size", "paged_decode_workspace_size",
-            "attn_check_device_status", "attn_reset_device_status", "attn_status_string", "attn_version"]
+            "attn_check_device_status", "attn_reset_device_status", "attn_status_string", "attn_version",
+            "paged_decode_attn_noalloc"]
 
 
 # --------------------------------------------------------------------------
@@ -315,4 +317,29 @@ def paged_kv_gather(cache: torch.Tensor, block_table: torch.Tensor, lens: torch.
                              block_table.shape[1], lens.data_ptr(), B, max_len, out.data_ptr(), ws.ptr, ws.nbytes,
                              _stream(stream))
     _check("paged_kv_gather", st)
+    return out
+
+
+def paged_decode_attn_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                              block_table: torch.Tensor, ctx_lens: torch.Tensor, scale: Optional[float] = None,
+                              out: torch.Tensor = None, lse: Optional[torch.Tensor] = None,
+                              device_status: Optional[torch.Tensor] = None, stream=None):
+    """paged_decode_attn for callers that cannot allocate device memory: the
+    split-K scratch is the library's built-in 20 MiB array, so `out` (and
+    `lse`, `device_status` if wanted) must be passed in.  Calls that overlap on
+    the GPU race on the shared scratch."""
+    lib = load()
+    B, Hq, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    assert out is not None, "the no-alloc call writes into a caller buffer"
+    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1
+    assert ctx_lens.dtype == torch.int32 and ctx_lens.is_contiguous()
+    c = _cache(k_cache, v_cache)
+    dq, do = _desc(q), _desc(out)
+    st = lib.paged_decode_attn_noalloc(ctypes.byref(dq), ctypes.byref(c), block_table.data_ptr(),
+                                       block_table.stride(0), block_table.shape[1], ctx_lens.data_ptr(),
+                                       float(scale), ctypes.byref(do), _ptr(lse), _ptr(device_status),
+                                       _stream(stream))
+    _check("paged_decode_attn_noalloc", st)
     return out
