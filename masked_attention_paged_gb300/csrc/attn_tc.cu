@@ -5,25 +5,30 @@
 // SDPA route with an additive -inf padding mask; "[sglang] ROCm aiter ring
 // attention", section 1, the LSE the merge needs): for each query row
 //   s_j = scale * q.k_j + mask_j,  out = sum_j softmax(s)_j v_j,  lse = log sum_j e^{s_j}
-// without ever storing the score matrix: one 128 x 128 score tile lives in
-// tensor memory at a time and is folded into the running output with the
-// online-softmax rescale.
+// without ever storing the score matrix: one 128 x 128 score tile per query
+// tile lives in tensor memory at a time and is folded into the running output
+// with the online-softmax rescale.
 //
-// CTA = one 128-row query tile of one (batch, head); 6 warps:
-//   warp 0      TMA producer: Q once, then K_j / V_j tiles into a ring of
-//               shared-memory stages (128-byte swizzle, 4-D tensor maps so the
-//               same code reads [B,H,P,D] and packed [T,H,D] layouts).
-//   warp 1      allocates TMEM; one lane issues tcgen05.mma:
-//                 S_j = Q K_j^T  (M=128, N=128, K=D)  into TMEM S[j%2]
-//                 O  += P_j V_j  (M=128, N=D,   K=128) into TMEM O
-//               and signals completion with tcgen05.commit -> mbarrier.
-//   warps 2-5   softmax: thread r owns row r (TMEM lane r).  Reads its S row
-//               from TMEM, adds the mask, keeps the running max/sum in the
-//               log2 domain, rescales O in TMEM when the max grows, writes
-//               P (bf16) to shared memory in the UMMA K-major swizzled layout,
-//               and finally normalises O and writes out / lse.
-// Order on the tensor pipe: S_0, S_1, PV_0, S_2, PV_1, ... so the softmax of
-// tile j+1 overlaps the PV of tile j.
+// CTA = two 128-row query tiles (A and B) of one (batch, head) sharing every
+// K/V tile; 3 warpgroups:
+//   warp 0      TMA producer: Q_A and Q_B once, then K_j / V_j tiles into a
+//               ring of shared-memory stages (128-byte swizzle; 4-D tensor maps
+//               so the same code reads [B,H,P,D] and packed [T,H,D] layouts).
+//   warp 1      allocates all 512 TMEM columns; one lane issues tcgen05.mma:
+//                 S_t = Q_t K_j^T  (M=128, N=128, K=D, both operands in smem)
+//                 O_t += P_t V_j   (M=128, N=D, K=128, P from TMEM, V in smem)
+//               in the order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), ... so the
+//               tensor pipe works on one tile while the other tile's softmax
+//               runs, and signals with tcgen05.commit -> mbarrier.
+//   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: thread r owns
+//               row r (TMEM lane r).  It reads its S row from TMEM, adds the
+//               mask, keeps the running max/sum in log2 units, writes P as
+//               bf16 pairs back into the first 64 columns of the same S
+//               region (the MMA that reads P precedes, in issue order, the
+//               next S MMA that overwrites it), rescales O in TMEM only when
+//               its reference max moves by more than kRescaleMargin, and
+//               finally normalises O and writes out / lse.
+// TMEM columns: S_A [0,128), S_B [128,256), O_A [256,256+D), O_B after it.
 //
 // Every wait is bounded (common.cuh): a hang turns into ATTN_ERR_TIMEOUT in
 // the caller's status word and the CTA winds down and frees its TMEM.
@@ -38,34 +43,37 @@
 namespace attn {
 namespace {
 
-constexpr int kBM = 128;       // query rows per CTA tile
+constexpr int kBM = 128;       // query rows per tile (two tiles per CTA)
 constexpr int kBN = 128;       // keys per KV tile
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kThreads = 384;  // 3 warpgroups
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
+__device__ __forceinline__ constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
 constexpr int kBoxBytes = kBM * 128;  // one 64-column (128-byte) box of 128 rows
+// A row's reference max (log2 units) only moves when the tile max exceeds it
+// by more than this; P then stays below 2^8, well inside bf16 and fp32 range.
+constexpr float kRescaleMargin = 8.0f;
 
 template <int D>
 struct Cfg {
   static constexpr int kBoxes = D / 64;
   static constexpr int kTileBytes = kBM * D * 2;
-  static constexpr int kStages = (D == 64) ? 3 : 2;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kTileBytes;
+  static constexpr int kStages = (D == 64) ? 4 : 2;
+  static constexpr uint32_t kColO0 = 256;
+  static constexpr int kOffQ = 0;  // Q_A, Q_B
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffP = kOffV + kStages * kTileBytes;
-  static constexpr int kOffMask = kOffP + kBM * kBN * 2;
-  static constexpr int kOffBar = kOffMask + 2 * kBN * 4;
+  static constexpr int kOffMask = kOffV + kStages * kTileBytes;  // [2 WG][2 buf][kBN] floats
+  static constexpr int kOffBar = kOffMask + 2 * 2 * kBN * 4;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + slack to align the base to 1024
 };
 
 struct Barriers {
   uint64_t q_full;
-  uint64_t k_full[3], k_empty[3];
-  uint64_t v_full[3], v_empty[3];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full, o_done, drain;
+  uint64_t k_full[4], k_empty[4];
+  uint64_t v_full[4], v_empty[4];
+  uint64_t s_full[2], p_full[2];
+  uint64_t o_final;
   uint32_t tmem_base;
   int abort;
 };
@@ -101,15 +109,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Barriers* bars = reinterpret_cast<Barriers*>(smem + C::kOffBar);
-  float* mask_buf = reinterpret_cast<float*>(smem + C::kOffMask);  // [2][kBN], log2 domain
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int q_tile = blockIdx.x;
   const int h = blockIdx.y;
   const int b = blockIdx.z;
   const int g = h / prm.group;
-  const int q0 = q_tile * kBM;
+  const int q0 = blockIdx.x * (2 * kBM);
   const int nkv = prm.n_kv_tiles;
   volatile int* abort = &bars->abort;
 
@@ -121,13 +127,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->v_full[s], 1);
       mbar_init(&bars->v_empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars->s_full[i], 1);
-      mbar_init(&bars->s_free[i], 4);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_full[t], 4);
     }
-    mbar_init(&bars->p_full, 4);
-    mbar_init(&bars->o_done, 1);
-    mbar_init(&bars->drain, 1);
+    mbar_init(&bars->o_final, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -140,6 +144,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  // Register budget: launched at 168 per thread (384 x 168 = 64512).  The
+  // producer/MMA warpgroup gives up 112 per thread (14336) and the two softmax
+  // warpgroups take 56 per thread (2 x 128 x 56 = 14336): the sum is unchanged.
+  if (warp < 4) regs_dec<56>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -147,11 +155,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       int c1, c2, c3;
-      mbar_arrive_expect_tx(&bars->q_full, C::kTileBytes);
-      coords(prm.cq, q0, h, b, c1, c2, c3);
+      mbar_arrive_expect_tx(&bars->q_full, 2 * C::kTileBytes);
 #pragma unroll
-      for (int x = 0; x < C::kBoxes; ++x)
-        tma_load_4d(smem + C::kOffQ + x * kBoxBytes, &tm_q, &bars->q_full, x * 64, c1, c2, c3);
+      for (int t = 0; t < 2; ++t) {
+        coords(prm.cq, q0 + t * kBM, h, b, c1, c2, c3);
+#pragma unroll
+        for (int x = 0; x < C::kBoxes; ++x)
+          tma_load_4d(smem + C::kOffQ + t * C::kTileBytes + x * kBoxBytes, &tm_q, &bars->q_full, x * 64, c1, c2,
+                      c3);
+      }
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < nkv; ++j) {
         const int s = j % C::kStages;
@@ -188,96 +200,117 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
       const uint32_t q_addr = smem_u32(smem + C::kOffQ);
-      const uint32_t p_addr = smem_u32(smem + C::kOffP);
-      bool ok = mbar_wait(&bars->q_full, 0, abort, prm.status);
-      tc_fence_after();
-      auto issue_pv = [&](int t) -> bool {
-        const int s = t % C::kStages;
-        const uint32_t ph = (t / C::kStages) & 1;
-        if (!mbar_wait(&bars->p_full, t & 1, abort, prm.status)) return false;
-        if (!mbar_wait(&bars->v_full[s], ph, abort, prm.status)) return false;
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(smem + C::kOffV + s * C::kTileBytes);
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          // A = P: K-major, 64-key column blocks of 16 KB, 32 bytes per k-step
-          const uint64_t a = sdesc_sw128(p_addr + (kk >> 2) * kBoxBytes + (kk & 3) * 32, 16, 1024);
-          // B = V: MN-major (d contiguous); 16 keys = two 8-row groups (SBO),
-          // next 64-column box of d at LBO
-          const uint64_t bd = sdesc_sw128(v_addr + kk * 2048, kBoxBytes, 1024);
-          umma_bf16_ss(tmem + kColO, a, bd, idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&bars->o_done);
-        umma_commit(&bars->v_empty[s]);
-        return true;
-      };
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int s = j % C::kStages;
-        const uint32_t ph = (j / C::kStages) & 1;
-        const int sb = j & 1;
-        if (!mbar_wait(&bars->k_full[s], ph, abort, prm.status)) { ok = false; break; }
-        if (j >= 2 && !mbar_wait(&bars->s_free[sb], ((j >> 1) & 1) ^ 1, abort, prm.status)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t k_addr = smem_u32(smem + C::kOffK + s * C::kTileBytes);
-        const uint32_t s_col = sb ? kColS1 : kColS0;
+      auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
+        const uint32_t k_addr = smem_u32(smem + C::kOffK + (j % C::kStages) * C::kTileBytes);
+        const uint32_t qa = q_addr + t * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-          const uint64_t a = sdesc_sw128(q_addr + off, 16, 1024);
-          const uint64_t bk = sdesc_sw128(k_addr + off, 16, 1024);
-          umma_bf16_ss(tmem + s_col, a, bk, idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;  // 16 dims = 32 bytes of a 128-byte row
+          umma_bf16_ss(tmem + col_s(t), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
+                       idesc_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&bars->s_full[sb]);
-        umma_commit(&bars->k_empty[s]);
-        if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+      };
+      auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j, P_t in TMEM
+        const uint32_t v_addr = smem_u32(smem + C::kOffV + (j % C::kStages) * C::kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          // 16 keys = 8 TMEM columns of packed P; V is MN-major (d contiguous):
+          // 16 keys = two 8-row groups (SBO), next 64-column box of d at LBO
+          umma_bf16_ts(tmem + C::kColO0 + t * D, tmem + col_s(t) + kk * 8,
+                       sdesc_sw128(v_addr + kk * 2048, kBoxBytes, 1024), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(&bars->q_full, 0, abort, prm.status);
+      if (ok && nkv > 0) {
+        ok = mbar_wait(&bars->k_full[0], 0, abort, prm.status);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, 0);
+          umma_commit(&bars->s_full[0]);
+          issue_s(1, 0);
+          umma_commit(&bars->s_full[1]);
+          umma_commit(&bars->k_empty[0]);
+        }
       }
-      if (ok && nkv > 0) issue_pv(nkv - 1);
-      // every MMA this thread issued must finish before TMEM is released
-      umma_commit(&bars->drain);
-      drain_wait(&bars->drain, 0);
+      for (int j = 0; ok && j < nkv; ++j) {
+        const int s = j % C::kStages;
+        const int j1 = j + 1;
+        const int s1 = j1 % C::kStages;
+        if (!mbar_wait(&bars->p_full[0], j & 1, abort, prm.status) ||
+            !mbar_wait(&bars->v_full[s], (j / C::kStages) & 1, abort, prm.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(0, j);
+        if (j1 < nkv) {
+          if (!mbar_wait(&bars->k_full[s1], (j1 / C::kStages) & 1, abort, prm.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_s(0, j1);  // issued after PV_A(j), which reads the P it overwrites
+          umma_commit(&bars->s_full[0]);
+        }
+        if (!mbar_wait(&bars->p_full[1], j & 1, abort, prm.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_pv(1, j);
+        umma_commit(&bars->v_empty[s]);
+        if (j1 < nkv) {
+          issue_s(1, j1);
+          umma_commit(&bars->s_full[1]);
+          umma_commit(&bars->k_empty[s1]);
+        }
+      }
+      // completes when every MMA above has: O is final and TMEM may be released
+      umma_commit(&bars->o_final);
+      drain_wait(&bars->o_final, 0);
     }
-  } else {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    const int wg_tid = threadIdx.x - 64;  // 0..127
-    const int quarter = warp & 3;         // TMEM lanes this warp may touch
-    const int row = quarter * 32 + lane;  // row within the tile == TMEM lane
+    regs_inc<224>();
+    const int t = (warp >> 2) - 1;            // query tile 0 (A) or 1 (B)
+    const int wg_tid = threadIdx.x - 128 * (t + 1);
+    const int quarter = warp & 3;             // TMEM lanes this warp may touch
+    const int row = quarter * 32 + lane;      // row within the tile == TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t s_col = col_s(t);
+    const uint32_t o_col = C::kColO0 + t * D;
+    float* mbuf = reinterpret_cast<float*>(smem + C::kOffMask) + t * 2 * kBN;
     const float kLog2e = 1.4426950408889634f;
     const float* mrow = prm.mask ? prm.mask + static_cast<int64_t>(b) * prm.mask_stride : nullptr;
     auto mask_at = [&](int key) -> float {
       if (key >= prm.Pk) return -INFINITY;
       return mrow ? mrow[key] * kLog2e : 0.0f;
     };
-    float m_run = -INFINITY;  // running max, log2 units
+    float m_run = -INFINITY;  // reference max, log2 units
     float l_run = 0.0f;       // running sum of 2^(x - m_run)
     float mreg = nkv > 0 ? mask_at(wg_tid) : 0.0f;
-    uint8_t* p_smem = smem + C::kOffP;
     bool ok = true;
 
     for (int j = 0; j < nkv; ++j) {
-      const int sb = j & 1;
-      mask_buf[sb * kBN + wg_tid] = mreg;
-      named_bar_sync(1, 128);
+      const int mb_i = j & 1;
+      mbuf[mb_i * kBN + wg_tid] = mreg;
+      named_bar_sync(1 + t, 128);
       if (j + 1 < nkv) mreg = mask_at((j + 1) * kBN + wg_tid);
       // wait outcomes are made warp-uniform: tcgen05.ld/st need the whole warp
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[sb], (j >> 1) & 1, abort, prm.status))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abort, prm.status))) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sr[4][32];
-      const uint32_t s_col = sb ? kColS1 : kColS0;
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_addr + s_col + c * 32, sr[c]);
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->s_free[sb]);
 
       // logits in log2 units with the additive mask (in place), tile max
       float mt = -INFINITY;
-      const float4* mb = reinterpret_cast<const float4*>(mask_buf + sb * kBN);
+      const float4* mb = reinterpret_cast<const float4*>(mbuf + mb_i * kBN);
 #pragma unroll
       for (int c4 = 0; c4 < kBN / 4; ++c4) {
         const float4 mv = mb[c4];
@@ -290,64 +323,55 @@ __global__ void __launch_bounds__(kThreads, 1)
           mt = fmaxf(mt, xv);
         }
       }
-      const float m_new = fmaxf(m_run, mt);
-      const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-      const float alpha = fast_exp2(m_run - m_use);  // 0 while nothing was unmasked
+      // lazy reference max: move it only when the tile exceeds it by the margin
+      float alpha = 1.0f;
+      if (mt > m_run + kRescaleMargin || (m_run == -INFINITY && mt != -INFINITY)) {
+        alpha = fast_exp2(m_run - mt);  // 0 when nothing was unmasked before
+        m_run = mt;
+      }
+      const float m_sub = (m_run == -INFINITY) ? 0.0f : m_run;
       float rs = 0.0f;
 #pragma unroll
       for (int c = 0; c < kBN; ++c) {
-        const float pv = fast_exp2(__uint_as_float(sr[c >> 5][c & 31]) - m_use);
+        const float pv = fast_exp2(__uint_as_float(sr[c >> 5][c & 31]) - m_sub);
         sr[c >> 5][c & 31] = __float_as_uint(pv);
         rs += pv;
       }
       l_run = l_run * alpha + rs;
-      m_run = m_new;
 
-      if (j > 0) {
-        // PV_{j-1} must be done: O is stable and the P buffer is free
-        if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_done, (j - 1) & 1, abort, prm.status))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+      // O_t is stable here: the commit behind s_full covers PV_t(j-1)
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tmem + lane_addr + kColO + c * 32, o);
-            tmem_wait_ld(o);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_addr + o_col + c * 32, o);
+          tmem_wait_ld(o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tmem + lane_addr + kColO + c * 32, o);
-          }
-          tmem_wait_st();
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tmem + lane_addr + o_col + c * 32, o);
         }
       }
-      // P (bf16) into the swizzled K-major operand layout: key chunk c of 8
-      // keys -> column block c/8, 16-byte slot (c%8) ^ (row%8) of the row
+      // P as bf16 pairs (key 2i in the low half) into the first 64 columns of S_t
 #pragma unroll
-      for (int c = 0; c < kBN / 8; ++c) {
-        const uint32_t* pr = &sr[c >> 2][(c & 3) * 8];
-        uint4 w;
-        w.x = pack_bf16x2(__uint_as_float(pr[0]), __uint_as_float(pr[1]));
-        w.y = pack_bf16x2(__uint_as_float(pr[2]), __uint_as_float(pr[3]));
-        w.z = pack_bf16x2(__uint_as_float(pr[4]), __uint_as_float(pr[5]));
-        w.w = pack_bf16x2(__uint_as_float(pr[6]), __uint_as_float(pr[7]));
-        uint8_t* dst = p_smem + (c >> 3) * kBoxBytes + row * 128 + ((((c & 7) ^ (row & 7))) << 4);
-        *reinterpret_cast<uint4*>(dst) = w;
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pw[i] = pack_bf16x2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
+        tmem_st16(tmem + lane_addr + s_col + c * 16, pw);
       }
-      fence_proxy_async_smem();
+      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_full);
+      if (lane == 0) mbar_arrive(&bars->p_full[t]);
     }
 
     // ---------------------------------------------------------- epilogue
     if (ok && nkv > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done, (nkv - 1) & 1, abort, prm.status));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_final, 0, abort, prm.status));
       tc_fence_after();
     }
-    const int qi = q0 + row;
+    const int qi = q0 + t * kBM + row;
     const bool empty = !(l_run > 0.0f);
     const float inv_l = empty ? 0.0f : 1.0f / l_run;
     const int64_t obase = static_cast<int64_t>(b) * prm.out_stride[0] + static_cast<int64_t>(h) * prm.out_stride[1] +
@@ -356,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
       if (ok && nkv > 0) {
-        tmem_ld32(tmem + lane_addr + kColO + c * 32, o);
+        tmem_ld32(tmem + lane_addr + o_col + c * 32, o);
         tmem_wait_ld(o);
       } else {
 #pragma unroll
@@ -487,7 +511,7 @@ cudaError_t launch_tc(const AttnFwdArgs& a, cudaStream_t stream) {
   const int smem = Cfg<D>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>((a.Pq + kBM - 1) / kBM), static_cast<unsigned>(a.Hq),
+  dim3 grid(static_cast<unsigned>((a.Pq + 2 * kBM - 1) / (2 * kBM)), static_cast<unsigned>(a.Hq),
             static_cast<unsigned>(a.B));
   kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
