@@ -86,6 +86,7 @@ struct TmaCoordMap {
 struct TcParams {
   int Pq, Pk, Hq, group, n_kv_tiles;
   float scale_log2;
+  int scale_positive;  // max of raw scores == max of scaled scores
   const float* mask;
   int64_t mask_stride;
   void* out;
@@ -294,7 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < nkv; ++j) {
       const int mb_i = j & 1;
       mbuf[mb_i * kBN + wg_tid] = mreg;
-      named_bar_sync(1 + t, 128);
+      // one barrier both publishes the tile's mask and tells whether any of
+      // its keys is masked (or past Pk)
+      const bool masked_tile = named_bar_or(1 + t, 128, mreg != 0.0f) || !prm.scale_positive;
       if (j + 1 < nkv) mreg = mask_at((j + 1) * kBN + wg_tid);
       // wait outcomes are made warp-uniform: tcgen05.ld/st need the whole warp
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abort, prm.status))) {
@@ -308,21 +311,34 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
 
-      // logits in log2 units with the additive mask (in place), tile max
-      float mt = -INFINITY;
-      const float4* mb = reinterpret_cast<const float4*>(mbuf + mb_i * kBN);
+      // tile max in log2 units; 8 independent partial maxima keep the chain short
+      float mx[8];
+      if (!masked_tile) {
+        // no masked key: the max of the raw scores, scaled once (scale > 0)
 #pragma unroll
-      for (int c4 = 0; c4 < kBN / 4; ++c4) {
-        const float4 mv = mb[c4];
-        const float madd[4] = {mv.x, mv.y, mv.z, mv.w};
+        for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(sr[0][i]);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int c = 4 * c4 + e;
-          const float xv = fmaf(__uint_as_float(sr[c >> 5][c & 31]), prm.scale_log2, madd[e]);
-          sr[c >> 5][c & 31] = __float_as_uint(xv);
-          mt = fmaxf(mt, xv);
+        for (int c = 8; c < kBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sr[c >> 5][c & 31]));
+      } else {
+        // logits with the additive mask, in place
+        const float4* mb = reinterpret_cast<const float4*>(mbuf + mb_i * kBN);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+        for (int c4 = 0; c4 < kBN / 4; ++c4) {
+          const float4 mv = mb[c4];
+          const float madd[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * c4 + e;
+            const float xv = fmaf(__uint_as_float(sr[c >> 5][c & 31]), prm.scale_log2, madd[e]);
+            sr[c >> 5][c & 31] = __float_as_uint(xv);
+            mx[c & 7] = fmaxf(mx[c & 7], xv);
+          }
         }
       }
+      float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      if (!masked_tile) mt *= prm.scale_log2;
       // lazy reference max: move it only when the tile exceeds it by the margin
       float alpha = 1.0f;
       if (mt > m_run + kRescaleMargin || (m_run == -INFINITY && mt != -INFINITY)) {
@@ -330,15 +346,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_run = mt;
       }
       const float m_sub = (m_run == -INFINITY) ? 0.0f : m_run;
-      float rs = 0.0f;
+      float rsum[8];
 #pragma unroll
-      for (int c = 0; c < kBN; ++c) {
-        const float pv = fast_exp2(__uint_as_float(sr[c >> 5][c & 31]) - m_sub);
-        sr[c >> 5][c & 31] = __float_as_uint(pv);
-        rs += pv;
+      for (int i = 0; i < 8; ++i) rsum[i] = 0.0f;
+      if (!masked_tile) {
+        const float neg = -m_sub;
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          const float pv = fast_exp2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), prm.scale_log2, neg));
+          sr[c >> 5][c & 31] = __float_as_uint(pv);
+          rsum[c & 7] += pv;
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          const float pv = fast_exp2(__uint_as_float(sr[c >> 5][c & 31]) - m_sub);  // -inf -> 0
+          sr[c >> 5][c & 31] = __float_as_uint(pv);
+          rsum[c & 7] += pv;
+        }
       }
+      const float rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) + ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
       l_run = l_run * alpha + rs;
 
+      // P as bf16 pairs (key 2i in the low half) into the first 64 columns of S_t
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pw[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pw[i] = pack_bf16x2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
+        tmem_st16(tmem + lane_addr + s_col + c * 16, pw);
+      }
       // O_t is stable here: the commit behind s_full covers PV_t(j-1)
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll
@@ -350,15 +388,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
           tmem_st32(tmem + lane_addr + o_col + c * 32, o);
         }
-      }
-      // P as bf16 pairs (key 2i in the low half) into the first 64 columns of S_t
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pw[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pw[i] = pack_bf16x2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
-        tmem_st16(tmem + lane_addr + s_col + c * 16, pw);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -499,6 +528,7 @@ cudaError_t launch_tc(const AttnFwdArgs& a, cudaStream_t stream) {
   p.group = static_cast<int>(a.Hq / a.Hkv);
   p.n_kv_tiles = static_cast<int>((a.Pk + kBN - 1) / kBN);
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  p.scale_positive = p.scale_log2 > 0.0f;
   p.mask = a.mask;
   p.mask_stride = a.mask_stride;
   p.out = a.out.data;
