@@ -55,6 +55,13 @@ constexpr float kRescaleMargin = 8.0f;
 
 template <int D>
 struct Cfg {
+  // D = 64 leaves room in TMEM for P apart from S (S_A, S_B 128 columns each,
+  // O_A, O_B 64 each, P_A, P_B 64 each = 512): the next S can then be issued
+  // as soon as the softmax has read the current one, and each softmax
+  // warpgroup runs tile after tile without waiting for its PV.  At D = 128
+  // P is written over the first half of its S region instead.
+  static constexpr bool kSepP = (D == 64);
+  static constexpr uint32_t kColP0 = 256 + 2 * D;  // P_A, P_B (kSepP only)
   static constexpr int kBoxes = D / 64;
   static constexpr int kTileBytes = kBM * D * 2;
   static constexpr int kStages = (D == 64) ? 4 : 2;
@@ -62,8 +69,8 @@ struct Cfg {
   static constexpr int kOffQ = 0;  // Q_A, Q_B
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffMask = kOffV + kStages * kTileBytes;  // [2 WG][2 buf][kBN] floats
-  static constexpr int kOffBar = kOffMask + 2 * 2 * kBN * 4;
+  static constexpr int kOffMask = kOffV + kStages * kTileBytes;  // [2 buf][kBN] floats, log2 units
+  static constexpr int kOffBar = kOffMask + 2 * kBN * 4;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + slack to align the base to 1024
 };
@@ -73,7 +80,10 @@ struct Barriers {
   uint64_t k_full[4], k_empty[4];
   uint64_t v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2];
+  uint64_t s_free[2], o_done[2];   // kSepP: S read out by the softmax; PV done
+  uint64_t m_full[2], m_empty[2];  // mask tile staging (warp 2 -> softmax warps)
   uint64_t o_final;
+  int m_flag[2];                   // tile has a masked key (or keys past Pk)
   uint32_t tmem_base;
   int abort;
 };
@@ -131,6 +141,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
       mbar_init(&bars->p_full[t], 4);
+      mbar_init(&bars->m_full[t], 1);
+      mbar_init(&bars->m_empty[t], 8);
+      mbar_init(&bars->s_free[t], 4);
+      mbar_init(&bars->o_done[t], 1);
     }
     mbar_init(&bars->o_final, 1);
     bars->abort = 0;
@@ -146,9 +160,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = bars->tmem_base;
 
   // Register budget: launched at 168 per thread (384 x 168 = 64512).  The
-  // producer/MMA warpgroup gives up 112 per thread (14336) and the two softmax
-  // warpgroups take 56 per thread (2 x 128 x 56 = 14336): the sum is unchanged.
-  if (warp < 4) regs_dec<56>();
+  // producer/MMA/mask warpgroup gives up 80 per thread (10240) and the two
+  // softmax warpgroups take 40 per thread (2 x 128 x 40 = 10240): the sum is
+  // unchanged.
+  if (warp < 4) regs_dec<88>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -213,11 +228,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j, P_t in TMEM
         const uint32_t v_addr = smem_u32(smem + C::kOffV + (j % C::kStages) * C::kTileBytes);
+        const uint32_t p_col = C::kSepP ? C::kColP0 + t * 64 : col_s(t);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           // 16 keys = 8 TMEM columns of packed P; V is MN-major (d contiguous):
           // 16 keys = two 8-row groups (SBO), next 64-column box of d at LBO
-          umma_bf16_ts(tmem + C::kColO0 + t * D, tmem + col_s(t) + kk * 8,
+          umma_bf16_ts(tmem + C::kColO0 + t * D, tmem + p_col + kk * 8,
                        sdesc_sw128(v_addr + kk * 2048, kBoxBytes, 1024), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
         }
       };
@@ -233,6 +249,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(&bars->k_empty[0]);
         }
       }
+      if constexpr (C::kSepP) {
+        // S_A(j+1) as soon as softmax A has read S_A(j); PV_A(j) once P_A(j)
+        // is written; then the same for B
+        for (int j = 0; ok && j < nkv; ++j) {
+          const int s = j % C::kStages;
+          const int j1 = j + 1;
+          const int s1 = j1 % C::kStages;
+          const bool more = j1 < nkv;
+          if (more && !mbar_wait(&bars->k_full[s1], (j1 / C::kStages) & 1, abort, prm.status)) { ok = false; break; }
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (more) {
+              if (!mbar_wait(&bars->s_free[t], j & 1, abort, prm.status)) { ok = false; break; }
+              tc_fence_after();
+              issue_s(t, j1);
+              umma_commit(&bars->s_full[t]);
+              if (t == 1) umma_commit(&bars->k_empty[s1]);
+            }
+            if (!mbar_wait(&bars->p_full[t], j & 1, abort, prm.status) ||
+                (t == 0 && !mbar_wait(&bars->v_full[s], (j / C::kStages) & 1, abort, prm.status))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(t, j);
+            umma_commit(&bars->o_done[t]);
+            if (t == 1) umma_commit(&bars->v_empty[s]);
+          }
+        }
+      } else {
       for (int j = 0; ok && j < nkv; ++j) {
         const int s = j % C::kStages;
         const int j1 = j + 1;
@@ -266,41 +312,55 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(&bars->k_empty[s1]);
         }
       }
+      }
       // completes when every MMA above has: O is final and TMEM may be released
       umma_commit(&bars->o_final);
       drain_wait(&bars->o_final, 0);
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ mask stager
+    // Each 128-key tile's additive mask, in log2 units (-inf past Pk), goes
+    // to a double-buffered shared array with a flag telling whether any of
+    // its keys is masked; both softmax warpgroups read it.
+    const float kLog2e = 1.4426950408889634f;
+    const float* mrow = prm.mask ? prm.mask + static_cast<int64_t>(b) * prm.mask_stride : nullptr;
+    float* mbuf = reinterpret_cast<float*>(smem + C::kOffMask);
+    for (int j = 0; j < nkv; ++j) {
+      const int s = j & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->m_empty[s], ((j >> 1) & 1) ^ 1, abort, prm.status))) break;
+      float v[4];
+      bool any = false;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = j * kBN + lane * 4 + e;
+        v[e] = key >= prm.Pk ? -INFINITY : (mrow ? mrow[key] * kLog2e : 0.0f);
+        any |= v[e] != 0.0f;
+      }
+      *reinterpret_cast<float4*>(mbuf + s * kBN + lane * 4) = make_float4(v[0], v[1], v[2], v[3]);
+      any = __any_sync(0xffffffffu, any);
+      if (lane == 0) bars->m_flag[s] = any || !prm.scale_positive;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->m_full[s]);
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    regs_inc<224>();
+    regs_inc<208>();
     const int t = (warp >> 2) - 1;            // query tile 0 (A) or 1 (B)
-    const int wg_tid = threadIdx.x - 128 * (t + 1);
     const int quarter = warp & 3;             // TMEM lanes this warp may touch
     const int row = quarter * 32 + lane;      // row within the tile == TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_col = col_s(t);
     const uint32_t o_col = C::kColO0 + t * D;
-    float* mbuf = reinterpret_cast<float*>(smem + C::kOffMask) + t * 2 * kBN;
-    const float kLog2e = 1.4426950408889634f;
-    const float* mrow = prm.mask ? prm.mask + static_cast<int64_t>(b) * prm.mask_stride : nullptr;
-    auto mask_at = [&](int key) -> float {
-      if (key >= prm.Pk) return -INFINITY;
-      return mrow ? mrow[key] * kLog2e : 0.0f;
-    };
+    const float* mbuf = reinterpret_cast<const float*>(smem + C::kOffMask);
     float m_run = -INFINITY;  // reference max, log2 units
     float l_run = 0.0f;       // running sum of 2^(x - m_run)
-    float mreg = nkv > 0 ? mask_at(wg_tid) : 0.0f;
     bool ok = true;
 
     for (int j = 0; j < nkv; ++j) {
       const int mb_i = j & 1;
-      mbuf[mb_i * kBN + wg_tid] = mreg;
-      // one barrier both publishes the tile's mask and tells whether any of
-      // its keys is masked (or past Pk)
-      const bool masked_tile = named_bar_or(1 + t, 128, mreg != 0.0f) || !prm.scale_positive;
-      if (j + 1 < nkv) mreg = mask_at((j + 1) * kBN + wg_tid);
       // wait outcomes are made warp-uniform: tcgen05.ld/st need the whole warp
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abort, prm.status))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abort, prm.status) &&
+                                       mbar_wait(&bars->m_full[mb_i], (j >> 1) & 1, abort, prm.status))) {
         ok = false;
         break;
       }
@@ -308,17 +368,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sr[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_addr + s_col + c * 32, sr[c]);
+      const bool masked_tile = bars->m_flag[mb_i] != 0;
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
+      if constexpr (C::kSepP) {  // S is in registers: the next S may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->s_free[t]);
+      }
+#define SV(c) __uint_as_float(sr[(c) >> 5][(c) & 31])
 
-      // tile max in log2 units; 8 independent partial maxima keep the chain short
+      // tile max in log2 units: 8 independent chains of 3-input max
       float mx[8];
       if (!masked_tile) {
         // no masked key: the max of the raw scores, scaled once (scale > 0)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(sr[0][i]);
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(SV(2 * i), SV(2 * i + 1));
 #pragma unroll
-        for (int c = 8; c < kBN; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(sr[c >> 5][c & 31]));
+        for (int c = 16; c < kBN; c += 2) mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], SV(c), SV(c + 1));
       } else {
         // logits with the additive mask, in place
         const float4* mb = reinterpret_cast<const float4*>(mbuf + mb_i * kBN);
@@ -327,17 +394,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c4 = 0; c4 < kBN / 4; ++c4) {
           const float4 mv = mb[c4];
-          const float madd[4] = {mv.x, mv.y, mv.z, mv.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 4 * c4 + e;
-            const float xv = fmaf(__uint_as_float(sr[c >> 5][c & 31]), prm.scale_log2, madd[e]);
-            sr[c >> 5][c & 31] = __float_as_uint(xv);
-            mx[c & 7] = fmaxf(mx[c & 7], xv);
-          }
+          const float x0 = fmaf(SV(4 * c4), prm.scale_log2, mv.x);
+          const float x1 = fmaf(SV(4 * c4 + 1), prm.scale_log2, mv.y);
+          const float x2 = fmaf(SV(4 * c4 + 2), prm.scale_log2, mv.z);
+          const float x3 = fmaf(SV(4 * c4 + 3), prm.scale_log2, mv.w);
+          sr[c4 >> 3][(4 * c4) & 31] = __float_as_uint(x0);
+          sr[c4 >> 3][(4 * c4 + 1) & 31] = __float_as_uint(x1);
+          sr[c4 >> 3][(4 * c4 + 2) & 31] = __float_as_uint(x2);
+          sr[c4 >> 3][(4 * c4 + 3) & 31] = __float_as_uint(x3);
+          mx[(2 * c4) & 7] = fmax3(mx[(2 * c4) & 7], x0, x1);
+          mx[(2 * c4 + 1) & 7] = fmax3(mx[(2 * c4 + 1) & 7], x2, x3);
         }
       }
-      float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->m_empty[mb_i]);  // this warp is done with the mask tile
+      float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       if (!masked_tile) mt *= prm.scale_log2;
       // lazy reference max: move it only when the tile exceeds it by the margin
       float alpha = 1.0f;
@@ -353,31 +424,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float neg = -m_sub;
 #pragma unroll
         for (int c = 0; c < kBN; ++c) {
-          const float pv = fast_exp2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), prm.scale_log2, neg));
+          const float pv = fast_exp2(fmaf(SV(c), prm.scale_log2, neg));
           sr[c >> 5][c & 31] = __float_as_uint(pv);
           rsum[c & 7] += pv;
         }
       } else {
 #pragma unroll
         for (int c = 0; c < kBN; ++c) {
-          const float pv = fast_exp2(__uint_as_float(sr[c >> 5][c & 31]) - m_sub);  // -inf -> 0
+          const float pv = fast_exp2(SV(c) - m_sub);  // -inf -> 0
           sr[c >> 5][c & 31] = __float_as_uint(pv);
           rsum[c & 7] += pv;
         }
       }
+#undef SV
       const float rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) + ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
       l_run = l_run * alpha + rs;
 
-      // P as bf16 pairs (key 2i in the low half) into the first 64 columns of S_t
+      if constexpr (C::kSepP) {
+        // P_t and O_t are free once PV_t(j-1) has completed
+        if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], (j - 1) & 1, abort, prm.status))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      // P as bf16 pairs (key 2i in the low half): its own region (D = 64) or
+      // the first 64 columns of S_t (D = 128)
+      const uint32_t p_col = C::kSepP ? C::kColP0 + t * 64 : s_col;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pw[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           pw[i] = pack_bf16x2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
-        tmem_st16(tmem + lane_addr + s_col + c * 16, pw);
+        tmem_st16(tmem + lane_addr + p_col + c * 16, pw);
       }
-      // O_t is stable here: the commit behind s_full covers PV_t(j-1)
+      // O_t is stable here: PV_t(j-1) has completed (o_done, or the commit
+      // behind s_full when P shares S's columns)
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
