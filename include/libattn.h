@@ -137,7 +137,8 @@ attn_status attn_fwd(const attn_tensor *q, const attn_tensor *k, const attn_tens
  *   out     [B, H, P, D] bf16 or f32; may alias outs[0] exactly (same
  *           data pointer and strides), must not overlap the other outs
  *   lse     float32 [B, H, P] contiguous, or NULL; must not overlap any lses[i]
- * D <= 256, D % 8 == 0; bases and dim-0..2 strides 16-byte aligned.
+ * D in {8, 16, ..., 64, 96, 128, 192, 256}; B, H <= 65535; bases and dim-0..2
+ * strides 16-byte aligned.
  */
 attn_status attn_lse_merge(int32_t n, const attn_tensor *outs, const float *const *lses,
                            const attn_tensor *out, float *lse, cudaStream_t stream);

@@ -173,7 +173,10 @@ attn_status attn_lse_merge(int32_t n, const attn_tensor* outs, const float* cons
       if (outs[i].shape[d] != out->shape[d]) return ATTN_ERR_INVALID_ARG;
     if (outs[i].dtype != outs[0].dtype) return ATTN_ERR_INVALID_ARG;
   }
-  if (D % 8 != 0 || D > 256 || D <= 0) return ATTN_ERR_UNSUPPORTED;
+  // head dims with a merge kernel instance: 8..64 in steps of 8, 96, 128, 192, 256
+  if (D % 8 != 0 || D > 256 || D <= 0 || (D > 64 && D != 96 && D != 128 && D != 192 && D != 256))
+    return ATTN_ERR_UNSUPPORTED;
+  if (B > 65535 || H > 65535) return ATTN_ERR_UNSUPPORTED;
   if (B * H * P == 0) return ATTN_OK;
   for (int i = 0; i < n; ++i) {
     if (lses[i] == nullptr || !aligned(lses[i], 4)) return ATTN_ERR_INVALID_ARG;

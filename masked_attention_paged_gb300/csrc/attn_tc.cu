@@ -14,12 +14,15 @@
 //   warp 0      TMA producer: Q_A and Q_B once, then K_j / V_j tiles into a
 //               ring of shared-memory stages (128-byte swizzle; 4-D tensor maps
 //               so the same code reads [B,H,P,D] and packed [T,H,D] layouts).
-//   warp 1      allocates all 512 TMEM columns; one lane issues tcgen05.mma:
+//   warp 1      allocates all 512 TMEM columns; lane 0 issues tcgen05.mma for
+//               tile A, lane 0 of warp 3 for tile B:
 //                 S_t = Q_t K_j^T  (M=128, N=128, K=D, both operands in smem)
 //                 O_t += P_t V_j   (M=128, N=D, K=128, P from TMEM, V in smem)
-//               in the order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1), ... so the
-//               tensor pipe works on one tile while the other tile's softmax
-//               runs, and signals with tcgen05.commit -> mbarrier.
+//               so the tensor pipe works on one tile while the other tile's
+//               softmax runs; completion is signalled with tcgen05.commit ->
+//               mbarrier, and a K/V stage is released after both issuers'
+//               commits.
+//   warp 2      stages each key tile's mask and a has-masked-keys flag.
 //   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: thread r owns
 //               row r (TMEM lane r).  It reads its S row from TMEM, adds the
 //               mask, keeps the running max/sum in log2 units, writes P as
@@ -61,6 +64,10 @@ struct Cfg {
   // warpgroup runs tile after tile without waiting for its PV.  At D = 128
   // P is written over the first half of its S region instead.
   static constexpr bool kSepP = (D == 64);
+  // With P apart from S each tile gets its own MMA-issuing warp; with P over
+  // S one warp issues both tiles in the order PV_A, S_A', PV_B, S_B', which
+  // keeps each tile's PV -> next-S chain short.
+  static constexpr bool kTwoIssuers = kSepP;
   static constexpr uint32_t kColP0 = 256 + 2 * D;  // P_A, P_B (kSepP only)
   static constexpr int kBoxes = D / 64;
   static constexpr int kTileBytes = kBM * D * 2;
@@ -71,7 +78,7 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
   static constexpr int kOffMask = kOffV + kStages * kTileBytes;  // [2 buf][kBN] floats, log2 units
   static constexpr int kOffBar = kOffMask + 2 * kBN * 4;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + slack to align the base to 1024
 };
 
@@ -82,11 +89,13 @@ struct Barriers {
   uint64_t s_full[2], p_full[2];
   uint64_t s_free[2], o_done[2];   // kSepP: S read out by the softmax; PV done
   uint64_t m_full[2], m_empty[2];  // mask tile staging (warp 2 -> softmax warps)
-  uint64_t o_final;
+  uint64_t o_final[2];
   int m_flag[2];                   // tile has a masked key (or keys past Pk)
   uint32_t tmem_base;
   int abort;
 };
+
+static_assert(sizeof(Barriers) <= 512, "barrier block outgrew its shared-memory slot");
 
 struct TmaCoordMap {
   // which tensor-map coordinate slot (1..3) carries the row, head and batch index
@@ -134,9 +143,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->q_full, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->k_full[s], 1);
-      mbar_init(&bars->k_empty[s], 1);
+      mbar_init(&bars->k_empty[s], C::kTwoIssuers ? 2 : 1);  // one commit per MMA issuer
       mbar_init(&bars->v_full[s], 1);
-      mbar_init(&bars->v_empty[s], 1);
+      mbar_init(&bars->v_empty[s], C::kTwoIssuers ? 2 : 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars->s_full[t], 1);
@@ -146,7 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->s_free[t], 4);
       mbar_init(&bars->o_done[t], 1);
     }
-    mbar_init(&bars->o_final, 1);
+    mbar_init(&bars->o_final[0], 1);
+    mbar_init(&bars->o_final[1], 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -210,15 +220,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           drain_wait(&bars->v_full[j % C::kStages], (j / C::kStages) & 1);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || (C::kTwoIssuers && warp == 3)) {
+    // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, false, false);
       constexpr uint32_t idesc_o = idesc_bf16_f32(kBM, D, false, true);
-      const uint32_t q_addr = smem_u32(smem + C::kOffQ);
       auto issue_s = [&](int t, int j) {  // S_t = Q_t K_j^T
+        const uint32_t qa = smem_u32(smem + C::kOffQ) + t * C::kTileBytes;
         const uint32_t k_addr = smem_u32(smem + C::kOffK + (j % C::kStages) * C::kTileBytes);
-        const uint32_t qa = q_addr + t * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;  // 16 dims = 32 bytes of a 128-byte row
@@ -228,18 +237,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_pv = [&](int t, int j) {  // O_t += P_t V_j, P_t in TMEM
         const uint32_t v_addr = smem_u32(smem + C::kOffV + (j % C::kStages) * C::kTileBytes);
-        const uint32_t p_col = C::kSepP ? C::kColP0 + t * 64 : col_s(t);
+        const uint32_t p_tmem = tmem + (C::kSepP ? C::kColP0 + t * 64 : col_s(t));
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           // 16 keys = 8 TMEM columns of packed P; V is MN-major (d contiguous):
           // 16 keys = two 8-row groups (SBO), next 64-column box of d at LBO
-          umma_bf16_ts(tmem + C::kColO0 + t * D, tmem + p_col + kk * 8,
-                       sdesc_sw128(v_addr + kk * 2048, kBoxBytes, 1024), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + C::kColO0 + t * D, p_tmem + kk * 8, sdesc_sw128(v_addr + kk * 2048, kBoxBytes, 1024),
+                       idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(&bars->q_full, 0, abort, prm.status);
-      if (ok && nkv > 0) {
-        ok = mbar_wait(&bars->k_full[0], 0, abort, prm.status);
+      bool ok = mbar_wait(&bars->q_full, 0, abort, prm.status) && nkv > 0 &&
+                mbar_wait(&bars->k_full[0], 0, abort, prm.status);
+      if constexpr (C::kTwoIssuers) {
+        // warp 1 issues every MMA of query tile A, warp 3 every MMA of tile B,
+        // so each tile's chain waits only on its own softmax warpgroup:
+        // S_t(j+1) as soon as the softmax has read S_t(j), PV_t(j) once P_t(j)
+        // is written
+        const int t = warp == 1 ? 0 : 1;
+        if (ok) {
+          tc_fence_after();
+          issue_s(t, 0);
+          umma_commit(&bars->s_full[t]);
+          umma_commit(&bars->k_empty[0]);
+        }
+        for (int j = 0; ok && j < nkv; ++j) {
+          const int s = j % C::kStages;
+          const int j1 = j + 1;
+          const int s1 = j1 % C::kStages;
+          if (j1 < nkv) {
+            if (!mbar_wait(&bars->k_full[s1], (j1 / C::kStages) & 1, abort, prm.status) ||
+                !mbar_wait(&bars->s_free[t], j & 1, abort, prm.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t, j1);
+            umma_commit(&bars->s_full[t]);
+            umma_commit(&bars->k_empty[s1]);
+          }
+          if (!mbar_wait(&bars->p_full[t], j & 1, abort, prm.status) ||
+              !mbar_wait(&bars->v_full[s], (j / C::kStages) & 1, abort, prm.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(t, j);
+          umma_commit(&bars->o_done[t]);
+          umma_commit(&bars->v_empty[s]);
+        }
+        // completes when every MMA of this tile has: O_t is final
+        umma_commit(&bars->o_final[t]);
+        drain_wait(&bars->o_final[t], 0);
+      } else {
+        // one issuer, order PV_A(j), S_A(j+1), PV_B(j), S_B(j+1): P_t(j) sits
+        // in S_t's columns and S_t(j+1) follows the PV_t(j) that reads it
+        // (one thread's MMAs execute in issue order)
         if (ok) {
           tc_fence_after();
           issue_s(0, 0);
@@ -248,74 +300,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(&bars->s_full[1]);
           umma_commit(&bars->k_empty[0]);
         }
-      }
-      if constexpr (C::kSepP) {
-        // S_A(j+1) as soon as softmax A has read S_A(j); PV_A(j) once P_A(j)
-        // is written; then the same for B
         for (int j = 0; ok && j < nkv; ++j) {
           const int s = j % C::kStages;
           const int j1 = j + 1;
           const int s1 = j1 % C::kStages;
-          const bool more = j1 < nkv;
-          if (more && !mbar_wait(&bars->k_full[s1], (j1 / C::kStages) & 1, abort, prm.status)) { ok = false; break; }
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (more) {
-              if (!mbar_wait(&bars->s_free[t], j & 1, abort, prm.status)) { ok = false; break; }
-              tc_fence_after();
-              issue_s(t, j1);
-              umma_commit(&bars->s_full[t]);
-              if (t == 1) umma_commit(&bars->k_empty[s1]);
-            }
-            if (!mbar_wait(&bars->p_full[t], j & 1, abort, prm.status) ||
-                (t == 0 && !mbar_wait(&bars->v_full[s], (j / C::kStages) & 1, abort, prm.status))) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_pv(t, j);
-            umma_commit(&bars->o_done[t]);
-            if (t == 1) umma_commit(&bars->v_empty[s]);
-          }
-        }
-      } else {
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int s = j % C::kStages;
-        const int j1 = j + 1;
-        const int s1 = j1 % C::kStages;
-        if (!mbar_wait(&bars->p_full[0], j & 1, abort, prm.status) ||
-            !mbar_wait(&bars->v_full[s], (j / C::kStages) & 1, abort, prm.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_pv(0, j);
-        if (j1 < nkv) {
-          if (!mbar_wait(&bars->k_full[s1], (j1 / C::kStages) & 1, abort, prm.status)) {
+          if (!mbar_wait(&bars->p_full[0], j & 1, abort, prm.status) ||
+              !mbar_wait(&bars->v_full[s], (j / C::kStages) & 1, abort, prm.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_s(0, j1);  // issued after PV_A(j), which reads the P it overwrites
-          umma_commit(&bars->s_full[0]);
+          issue_pv(0, j);
+          if (j1 < nkv) {
+            if (!mbar_wait(&bars->k_full[s1], (j1 / C::kStages) & 1, abort, prm.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(0, j1);
+            umma_commit(&bars->s_full[0]);
+          }
+          if (!mbar_wait(&bars->p_full[1], j & 1, abort, prm.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(1, j);
+          umma_commit(&bars->v_empty[s]);
+          if (j1 < nkv) {
+            issue_s(1, j1);
+            umma_commit(&bars->s_full[1]);
+            umma_commit(&bars->k_empty[s1]);
+          }
         }
-        if (!mbar_wait(&bars->p_full[1], j & 1, abort, prm.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_pv(1, j);
-        umma_commit(&bars->v_empty[s]);
-        if (j1 < nkv) {
-          issue_s(1, j1);
-          umma_commit(&bars->s_full[1]);
-          umma_commit(&bars->k_empty[s1]);
-        }
+        // completes when every MMA above has: O_A and O_B are final
+        umma_commit(&bars->o_final[0]);
+        umma_commit(&bars->o_final[1]);
+        drain_wait(&bars->o_final[1], 0);
       }
-      }
-      // completes when every MMA above has: O is final and TMEM may be released
-      umma_commit(&bars->o_final);
-      drain_wait(&bars->o_final, 0);
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ mask stager
@@ -480,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---------------------------------------------------------- epilogue
     if (ok && nkv > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_final, 0, abort, prm.status));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_final[t], 0, abort, prm.status));
       tc_fence_after();
     }
     const int qi = q0 + t * kBM + row;

@@ -137,50 +137,55 @@ __device__ __forceinline__ void load8(const void* base, int64_t off, bool bf16, 
   }
 }
 
-__global__ void lse_merge_kernel(const MergeParams p) {
-  const int vec = static_cast<int>(p.D / 8);
-  const int64_t total = p.rows * vec;
-  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = idx / vec;
-    const int c = static_cast<int>(idx % vec) * 8;
-    const int64_t pp = r % p.P, hh = (r / p.P) % p.H, bb = r / (p.P * p.H);
-    float l[8];
-    float M = -INFINITY;
-    for (int i = 0; i < p.n; ++i) {
-      l[i] = p.lses[i][r];
-      M = fmaxf(M, l[i]);
-    }
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float lse = -INFINITY;
-    if (M != -INFINITY) {
-      float tot = 0.f;
-      for (int i = 0; i < p.n; ++i) tot += expf(l[i] - M);
-      lse = M + logf(tot);
-      for (int i = 0; i < p.n; ++i) {
-        const float w = expf(l[i] - lse);
-        if (w == 0.f) continue;
-        float v[8];
-        load8(p.outs[i], bb * p.ostride[i][0] + hh * p.ostride[i][1] + pp * p.ostride[i][2] + c, p.in_bf16, v);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = fmaf(w, v[e], acc[e]);
-      }
-    }
-    const int64_t o = bb * p.out_stride[0] + hh * p.out_stride[1] + pp * p.out_stride[2] + c;
-    if (p.out_bf16) {
-      uint4 w;
-      w.x = pack_bf16x2(acc[0], acc[1]);
-      w.y = pack_bf16x2(acc[2], acc[3]);
-      w.z = pack_bf16x2(acc[4], acc[5]);
-      w.w = pack_bf16x2(acc[6], acc[7]);
-      *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + o) = w;
-    } else {
-      float4* f = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o);
-      f[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      f[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-    }
-    if (p.lse != nullptr && c == 0) p.lse[r] = lse;
+// One CTA covers kRows consecutive query rows of one (b, h); a row is D/8
+// threads, each moving 8 elements (16 bytes of bf16).  The weights are
+// computed in log2 units: w_i = 2^((lse_i - lse) * log2 e).
+constexpr int kMergeRows = 16;
+
+template <int VEC>  // threads per row = D / 8
+__global__ void __launch_bounds__(kMergeRows * VEC) lse_merge_kernel(const MergeParams p) {
+  const float kLog2e = 1.4426950408889634f;
+  const int64_t pp = static_cast<int64_t>(blockIdx.x) * kMergeRows + threadIdx.x / VEC;
+  if (pp >= p.P) return;
+  const int64_t hh = blockIdx.y, bb = blockIdx.z;
+  const int c = (threadIdx.x % VEC) * 8;
+  const int64_t r = (bb * p.H + hh) * p.P + pp;  // row of the contiguous LSE layout
+  float l2[8];
+  float M = -INFINITY;
+  for (int i = 0; i < p.n; ++i) {
+    l2[i] = p.lses[i][r] * kLog2e;
+    M = fmaxf(M, l2[i]);
   }
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float lse = -INFINITY;
+  if (M != -INFINITY) {
+    float tot = 0.f;
+    for (int i = 0; i < p.n; ++i) tot += fast_exp2(l2[i] - M);  // -inf -> 0
+    const float lse2 = M + __log2f(tot);
+    lse = lse2 * 0.6931471805599453f;
+    for (int i = 0; i < p.n; ++i) {
+      const float w = fast_exp2(l2[i] - lse2);
+      if (w == 0.f) continue;
+      float v[8];
+      load8(p.outs[i], bb * p.ostride[i][0] + hh * p.ostride[i][1] + pp * p.ostride[i][2] + c, p.in_bf16, v);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = fmaf(w, v[e], acc[e]);
+    }
+  }
+  const int64_t o = bb * p.out_stride[0] + hh * p.out_stride[1] + pp * p.out_stride[2] + c;
+  if (p.out_bf16) {
+    uint4 w;
+    w.x = pack_bf16x2(acc[0], acc[1]);
+    w.y = pack_bf16x2(acc[2], acc[3]);
+    w.z = pack_bf16x2(acc[4], acc[5]);
+    w.w = pack_bf16x2(acc[6], acc[7]);
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + o) = w;
+  } else {
+    float4* f = reinterpret_cast<float4*>(static_cast<float*>(p.out) + o);
+    f[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    f[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+  if (p.lse != nullptr && c == 0) p.lse[r] = lse;
 }
 
 // ---------------------------------------------------------------------------
@@ -267,14 +272,25 @@ cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t stream) {
   p.out_stride[2] = a.out.stride[2];
   p.out_bf16 = a.out.dtype == ATTN_BF16;
   p.lse = a.lse;
-  const int64_t threads_total = p.rows * (a.D / 8);
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int64_t want = (threads_total + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(sms) * 16;
-  const unsigned blocks = static_cast<unsigned>(std::max<int64_t>(1, std::min(want, cap)));
-  lse_merge_kernel<<<blocks, 256, 0, stream>>>(p);
+  const int vec = static_cast<int>(a.D / 8);
+  if (a.H > 65535 || a.B > 65535) return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>((a.P + kMergeRows - 1) / kMergeRows), static_cast<unsigned>(a.H),
+            static_cast<unsigned>(a.B));
+  switch (vec) {
+    case 1: lse_merge_kernel<1><<<grid, kMergeRows * 1, 0, stream>>>(p); break;
+    case 2: lse_merge_kernel<2><<<grid, kMergeRows * 2, 0, stream>>>(p); break;
+    case 3: lse_merge_kernel<3><<<grid, kMergeRows * 3, 0, stream>>>(p); break;
+    case 4: lse_merge_kernel<4><<<grid, kMergeRows * 4, 0, stream>>>(p); break;
+    case 5: lse_merge_kernel<5><<<grid, kMergeRows * 5, 0, stream>>>(p); break;
+    case 6: lse_merge_kernel<6><<<grid, kMergeRows * 6, 0, stream>>>(p); break;
+    case 7: lse_merge_kernel<7><<<grid, kMergeRows * 7, 0, stream>>>(p); break;
+    case 8: lse_merge_kernel<8><<<grid, kMergeRows * 8, 0, stream>>>(p); break;
+    case 12: lse_merge_kernel<12><<<grid, kMergeRows * 12, 0, stream>>>(p); break;
+    case 16: lse_merge_kernel<16><<<grid, kMergeRows * 16, 0, stream>>>(p); break;
+    case 24: lse_merge_kernel<24><<<grid, kMergeRows * 24, 0, stream>>>(p); break;
+    case 32: lse_merge_kernel<32><<<grid, kMergeRows * 32, 0, stream>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
