@@ -400,66 +400,98 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #define SV(c) __uint_as_float(sr[(c) >> 5][(c) & 31])
 
-      // tile max in log2 units: 8 independent chains of 3-input max
-      float mx[8];
-      if (!masked_tile) {
-        // no masked key: the max of the raw scores, scaled once (scale > 0)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(SV(2 * i), SV(2 * i + 1));
-#pragma unroll
-        for (int c = 16; c < kBN; c += 2) mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], SV(c), SV(c + 1));
-      } else {
-        // logits with the additive mask, in place
-        const float4* mb = reinterpret_cast<const float4*>(mbuf + mb_i * kBN);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-#pragma unroll
-        for (int c4 = 0; c4 < kBN / 4; ++c4) {
-          const float4 mv = mb[c4];
-          const float x0 = fmaf(SV(4 * c4), prm.scale_log2, mv.x);
-          const float x1 = fmaf(SV(4 * c4 + 1), prm.scale_log2, mv.y);
-          const float x2 = fmaf(SV(4 * c4 + 2), prm.scale_log2, mv.z);
-          const float x3 = fmaf(SV(4 * c4 + 3), prm.scale_log2, mv.w);
-          sr[c4 >> 3][(4 * c4) & 31] = __float_as_uint(x0);
-          sr[c4 >> 3][(4 * c4 + 1) & 31] = __float_as_uint(x1);
-          sr[c4 >> 3][(4 * c4 + 2) & 31] = __float_as_uint(x2);
-          sr[c4 >> 3][(4 * c4 + 3) & 31] = __float_as_uint(x3);
-          mx[(2 * c4) & 7] = fmax3(mx[(2 * c4) & 7], x0, x1);
-          mx[(2 * c4 + 1) & 7] = fmax3(mx[(2 * c4 + 1) & 7], x2, x3);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->m_empty[mb_i]);  // this warp is done with the mask tile
-      float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-      if (!masked_tile) mt *= prm.scale_log2;
-      // lazy reference max: move it only when the tile exceeds it by the margin
       float alpha = 1.0f;
-      if (mt > m_run + kRescaleMargin || (m_run == -INFINITY && mt != -INFINITY)) {
-        alpha = fast_exp2(m_run - mt);  // 0 when nothing was unmasked before
-        m_run = mt;
+      float rs = 0.0f;
+      bool done = false;
+      if constexpr (!C::kSepP) {
+        // Fast path: exponentiate against the current reference max without a
+        // max pass.  Every term is <= 2^64 exactly when the row sum is, which
+        // keeps the sums far from fp32 overflow; if some row fails, the warp
+        // reloads S (its columns are intact until P is written over them) and
+        // takes the full path below.
+        if (!masked_tile && __all_sync(0xffffffffu, m_run != -INFINITY)) {
+          float rsum[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) rsum[i] = 0.0f;
+          const float neg = -m_run;
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) {
+            const float pv = fast_exp2(fmaf(SV(c), prm.scale_log2, neg));
+            sr[c >> 5][c & 31] = __float_as_uint(pv);
+            rsum[c & 7] += pv;
+          }
+          rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) + ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
+          if (__all_sync(0xffffffffu, rs <= 18446744073709551616.0f)) {  // 2^64; false for NaN
+            done = true;
+          } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_addr + s_col + c * 32, sr[c]);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
+          }
+        }
       }
-      const float m_sub = (m_run == -INFINITY) ? 0.0f : m_run;
-      float rsum[8];
+      if (!done) {
+        // tile max in log2 units: 8 independent chains of 3-input max
+        float mx[8];
+        if (!masked_tile) {
+          // no masked key: the max of the raw scores, scaled once (scale > 0)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) rsum[i] = 0.0f;
-      if (!masked_tile) {
-        const float neg = -m_sub;
+          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(SV(2 * i), SV(2 * i + 1));
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          const float pv = fast_exp2(fmaf(SV(c), prm.scale_log2, neg));
-          sr[c >> 5][c & 31] = __float_as_uint(pv);
-          rsum[c & 7] += pv;
+          for (int c = 16; c < kBN; c += 2) mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], SV(c), SV(c + 1));
+        } else {
+          // logits with the additive mask, in place
+          const float4* mb = reinterpret_cast<const float4*>(mbuf + mb_i * kBN);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+          for (int c4 = 0; c4 < kBN / 4; ++c4) {
+            const float4 mv = mb[c4];
+            const float x0 = fmaf(SV(4 * c4), prm.scale_log2, mv.x);
+            const float x1 = fmaf(SV(4 * c4 + 1), prm.scale_log2, mv.y);
+            const float x2 = fmaf(SV(4 * c4 + 2), prm.scale_log2, mv.z);
+            const float x3 = fmaf(SV(4 * c4 + 3), prm.scale_log2, mv.w);
+            sr[c4 >> 3][(4 * c4) & 31] = __float_as_uint(x0);
+            sr[c4 >> 3][(4 * c4 + 1) & 31] = __float_as_uint(x1);
+            sr[c4 >> 3][(4 * c4 + 2) & 31] = __float_as_uint(x2);
+            sr[c4 >> 3][(4 * c4 + 3) & 31] = __float_as_uint(x3);
+            mx[(2 * c4) & 7] = fmax3(mx[(2 * c4) & 7], x0, x1);
+            mx[(2 * c4 + 1) & 7] = fmax3(mx[(2 * c4 + 1) & 7], x2, x3);
+          }
         }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          const float pv = fast_exp2(SV(c) - m_sub);  // -inf -> 0
-          sr[c >> 5][c & 31] = __float_as_uint(pv);
-          rsum[c & 7] += pv;
+        float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+        if (!masked_tile) mt *= prm.scale_log2;
+        // lazy reference max: move it only when the tile exceeds it by the margin
+        if (mt > m_run + kRescaleMargin || (m_run == -INFINITY && mt != -INFINITY)) {
+          alpha = fast_exp2(m_run - mt);  // 0 when nothing was unmasked before
+          m_run = mt;
         }
+        const float m_sub = (m_run == -INFINITY) ? 0.0f : m_run;
+        float rsum[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rsum[i] = 0.0f;
+        if (!masked_tile) {
+          const float neg = -m_sub;
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) {
+            const float pv = fast_exp2(fmaf(SV(c), prm.scale_log2, neg));
+            sr[c >> 5][c & 31] = __float_as_uint(pv);
+            rsum[c & 7] += pv;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) {
+            const float pv = fast_exp2(SV(c) - m_sub);  // -inf -> 0
+            sr[c >> 5][c & 31] = __float_as_uint(pv);
+            rsum[c & 7] += pv;
+          }
+        }
+        rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) + ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
       }
 #undef SV
-      const float rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) + ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->m_empty[mb_i]);  // this warp is done with the mask tile
       l_run = l_run * alpha + rs;
 
       if constexpr (C::kSepP) {

@@ -137,39 +137,48 @@ __device__ __forceinline__ void load8(const void* base, int64_t off, bool bf16, 
   }
 }
 
-// One CTA covers kRows consecutive query rows of one (b, h); a row is D/8
-// threads, each moving 8 elements (16 bytes of bf16).  The weights are
-// computed in log2 units: w_i = 2^((lse_i - lse) * log2 e).
-constexpr int kMergeRows = 16;
-
-template <int VEC>  // threads per row = D / 8
-__global__ void __launch_bounds__(kMergeRows * VEC) lse_merge_kernel(const MergeParams p) {
+// One CTA covers `rows` = 256 / (D/8) consecutive query rows of one (b, h);
+// a row is D/8 threads, each moving 8 elements (16 bytes of bf16).  NP (the number of
+// partials) is a template parameter so the prefetched values fit registers
+// exactly; every load is issued before any result is needed.  The weights
+// are computed in log2 units: w_i = 2^((lse_i - lse) * log2 e).
+template <int NP>
+__global__ void __launch_bounds__(256) lse_merge_kernel(const MergeParams p, int vec, int rows) {
   const float kLog2e = 1.4426950408889634f;
-  const int64_t pp = static_cast<int64_t>(blockIdx.x) * kMergeRows + threadIdx.x / VEC;
-  if (pp >= p.P) return;
+  const int row_in_cta = static_cast<int>(threadIdx.x) / vec;
+  const int64_t pp = static_cast<int64_t>(blockIdx.x) * rows + row_in_cta;
+  if (row_in_cta >= rows || pp >= p.P) return;
   const int64_t hh = blockIdx.y, bb = blockIdx.z;
-  const int c = (threadIdx.x % VEC) * 8;
+  const int c = (static_cast<int>(threadIdx.x) - row_in_cta * vec) * 8;
   const int64_t r = (bb * p.H + hh) * p.P + pp;  // row of the contiguous LSE layout
-  float l2[8];
+  float l2[NP];
+  float v[NP][8];
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    l2[i] = p.lses[i][r];
+    load8(p.outs[i], bb * p.ostride[i][0] + hh * p.ostride[i][1] + pp * p.ostride[i][2] + c, p.in_bf16, v[i]);
+  }
   float M = -INFINITY;
-  for (int i = 0; i < p.n; ++i) {
-    l2[i] = p.lses[i][r] * kLog2e;
+#pragma unroll
+  for (int i = 0; i < NP; ++i) {
+    l2[i] *= kLog2e;
     M = fmaxf(M, l2[i]);
   }
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   float lse = -INFINITY;
   if (M != -INFINITY) {
     float tot = 0.f;
-    for (int i = 0; i < p.n; ++i) tot += fast_exp2(l2[i] - M);  // -inf -> 0
+#pragma unroll
+    for (int i = 0; i < NP; ++i) tot += fast_exp2(l2[i] - M);  // -inf -> 0
     const float lse2 = M + __log2f(tot);
     lse = lse2 * 0.6931471805599453f;
-    for (int i = 0; i < p.n; ++i) {
-      const float w = fast_exp2(l2[i] - lse2);
-      if (w == 0.f) continue;
-      float v[8];
-      load8(p.outs[i], bb * p.ostride[i][0] + hh * p.ostride[i][1] + pp * p.ostride[i][2] + c, p.in_bf16, v);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = fmaf(w, v[e], acc[e]);
+    for (int i = 0; i < NP; ++i) {
+      const float w = fast_exp2(l2[i] - lse2);
+      if (w != 0.f) {  // a partial with no keys may hold anything
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(w, v[i][e], acc[e]);
+      }
     }
   }
   const int64_t o = bb * p.out_stride[0] + hh * p.out_stride[1] + pp * p.out_stride[2] + c;
@@ -272,23 +281,20 @@ cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t stream) {
   p.out_stride[2] = a.out.stride[2];
   p.out_bf16 = a.out.dtype == ATTN_BF16;
   p.lse = a.lse;
-  const int vec = static_cast<int>(a.D / 8);
+  const int vec = static_cast<int>(a.D / 8);  // threads per row, <= 32
   if (a.H > 65535 || a.B > 65535) return cudaErrorInvalidValue;
-  dim3 grid(static_cast<unsigned>((a.P + kMergeRows - 1) / kMergeRows), static_cast<unsigned>(a.H),
-            static_cast<unsigned>(a.B));
-  switch (vec) {
-    case 1: lse_merge_kernel<1><<<grid, kMergeRows * 1, 0, stream>>>(p); break;
-    case 2: lse_merge_kernel<2><<<grid, kMergeRows * 2, 0, stream>>>(p); break;
-    case 3: lse_merge_kernel<3><<<grid, kMergeRows * 3, 0, stream>>>(p); break;
-    case 4: lse_merge_kernel<4><<<grid, kMergeRows * 4, 0, stream>>>(p); break;
-    case 5: lse_merge_kernel<5><<<grid, kMergeRows * 5, 0, stream>>>(p); break;
-    case 6: lse_merge_kernel<6><<<grid, kMergeRows * 6, 0, stream>>>(p); break;
-    case 7: lse_merge_kernel<7><<<grid, kMergeRows * 7, 0, stream>>>(p); break;
-    case 8: lse_merge_kernel<8><<<grid, kMergeRows * 8, 0, stream>>>(p); break;
-    case 12: lse_merge_kernel<12><<<grid, kMergeRows * 12, 0, stream>>>(p); break;
-    case 16: lse_merge_kernel<16><<<grid, kMergeRows * 16, 0, stream>>>(p); break;
-    case 24: lse_merge_kernel<24><<<grid, kMergeRows * 24, 0, stream>>>(p); break;
-    case 32: lse_merge_kernel<32><<<grid, kMergeRows * 32, 0, stream>>>(p); break;
+  const int rows = 256 / vec;
+  const int threads = rows * vec;
+  dim3 grid(static_cast<unsigned>((a.P + rows - 1) / rows), static_cast<unsigned>(a.H), static_cast<unsigned>(a.B));
+  switch (a.n) {
+    case 1: lse_merge_kernel<1><<<grid, threads, 0, stream>>>(p, vec, rows); break;
+    case 2: lse_merge_kernel<2><<<grid, threads, 0, stream>>>(p, vec, rows); break;
+    case 3: lse_merge_kernel<3><<<grid, threads, 0, stream>>>(p, vec, rows); break;
+    case 4: lse_merge_kernel<4><<<grid, threads, 0, stream>>>(p, vec, rows); break;
+    case 5: lse_merge_kernel<5><<<grid, threads, 0, stream>>>(p, vec, rows); break;
+    case 6: lse_merge_kernel<6><<<grid, threads, 0, stream>>>(p, vec, rows); break;
+    case 7: lse_merge_kernel<7><<<grid, threads, 0, stream>>>(p, vec, rows); break;
+    case 8: lse_merge_kernel<8><<<grid, threads, 0, stream>>>(p, vec, rows); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
