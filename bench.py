@@ -59,18 +59,20 @@ def peaks():
 
 
 def traffic(kernel):
-    """DRAM bytes per launch from the committed ncu capture, or None when the
-    kernel's source changed since the counters were taken."""
+    """DRAM bytes per launch from the committed ncu capture, or None when any
+    source the kernel is compiled from changed since the counters were taken."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f)[kernel]
-        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        m = hashlib.sha256()
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                m.update(f.read())
     except (OSError, KeyError, ValueError):
         return None
-    return rec["bytes_per_launch"] if sha == rec["sha256_16"] else None
+    return rec["bytes_per_launch"] if m.hexdigest()[:16] == rec["sha256_16"] else None
 
 
 # ---------------------------------------------------------------------------
@@ -440,7 +442,8 @@ def main():
         "paged_decode_attn": {"ms": seg["decode"], "kv_gbs": step.kv_bytes / (seg["decode"] * 1e-3) / 1e9,
                               "gbs": dec_gbs, "frac": dec_gbs / pk["hbm_gbs"]},
         "kv_append": {"ms": seg["append"]},
-        "attn_lse_merge": {"ms": seg["merge"], "gbs": merge_gbs, "frac": merge_gbs / pk["hbm_gbs"]},
+        "attn_lse_merge": {"ms": seg["merge"], "gbs": merge_gbs, "frac": merge_gbs / pk["hbm_gbs"],
+                           "traffic": traffic("lse_merge_kernel")},
     }
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
