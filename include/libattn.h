@@ -238,6 +238,15 @@ attn_status paged_kv_gather(const attn_kv_cache *cache, int32_t which,
                             const int32_t *lens, int32_t batch, int64_t max_len, void *dst,
                             void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Self-test of the device-side hang guard: launches one thread that waits on
+ * a barrier phase nothing ever completes.  The wait gives up after
+ * timeout_us microseconds (1 .. 1000000), ORs ATTN_ERR_TIMEOUT into the
+ * workspace's status word and the kernel returns; the CUDA context stays
+ * usable.  Every pipeline wait in the library's kernels uses the same guard
+ * (with a 2 s limit). */
+attn_status attn_selftest_wait_timeout(void *workspace, size_t workspace_bytes, uint32_t timeout_us,
+                                       cudaStream_t stream);
+
 /* Copy the workspace's status word to the host (synchronises `stream`).
  * Returns ATTN_OK or the lowest-numbered error recorded since the last reset;
  * *raw (if not NULL) receives the full bit set, bit e meaning status e. */

@@ -87,6 +87,7 @@ def load(build_if_missing: bool = False):
             "paged_decode_attn_noalloc": (I32, [T, C, P, I64, I32, P, F, T, P, P, P]),
             "attn_check_device_status": (I32, [P, ctypes.POINTER(ctypes.c_uint32), P]),
             "attn_reset_device_status": (I32, [P, P]),
+            "attn_selftest_wait_timeout": (I32, [P, SZ, ctypes.c_uint32, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -100,7 +101,7 @@ def exported_symbols() -> list[str]:
     return ["attn_fwd", "attn_lse_merge", "kv_append", "paged_decode_attn", "paged_kv_gather",
             "attn_fwd_workspace_size", "kv_append_workspace_size", "paged_decode_workspace_size",
             "attn_check_device_status", "attn_reset_device_status", "attn_status_string", "attn_version",
-            "paged_decode_attn_noalloc"]
+            "paged_decode_attn_noalloc", "attn_selftest_wait_timeout"]
 
 
 # --------------------------------------------------------------------------

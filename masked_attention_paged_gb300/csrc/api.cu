@@ -300,6 +300,15 @@ attn_status paged_decode_attn(const attn_tensor* q, const attn_kv_cache* cache, 
   return from_cuda(launch_paged_decode(a, stream));
 }
 
+attn_status attn_selftest_wait_timeout(void* workspace, size_t workspace_bytes, uint32_t timeout_us,
+                                       cudaStream_t stream) {
+  attn_status st;
+  if ((st = check_workspace(workspace, workspace_bytes, kStatusBytes)) != ATTN_OK) return st;
+  if (timeout_us == 0 || timeout_us > 1000000u) return ATTN_ERR_INVALID_ARG;
+  return from_cuda(launch_wait_timeout_selftest(static_cast<uint32_t*>(workspace),
+                                                static_cast<uint64_t>(timeout_us) * 1000u, stream));
+}
+
 attn_status attn_check_device_status(const void* workspace, uint32_t* raw, cudaStream_t stream) {
   if (workspace == nullptr) return ATTN_ERR_WORKSPACE;
   uint32_t word = 0;

@@ -132,13 +132,13 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // by the hardware rather than spinning, so a waiting role takes no issue
 // slots from the roles sharing its SM sub-partition.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* status) {
+                                          uint32_t* status, uint64_t timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity, 200000u)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitTimeoutNs) {
+    if (globaltimer_ns() - t0 > timeout_ns) {
       *abort = 1;
       report(status, kStatusTimeout);
       return false;

@@ -99,4 +99,7 @@ int decode_num_splits(int max_blocks, int block_size);
 size_t decode_partial_bytes(int64_t B, int64_t Hq, int n_split, int D);
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);
 
+// one bounded mbarrier wait that nothing completes (exercises the timeout path)
+cudaError_t launch_wait_timeout_selftest(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);
+
 }  // namespace attn

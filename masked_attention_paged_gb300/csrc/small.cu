@@ -311,3 +311,30 @@ cudaError_t launch_attn_empty_keys(const AttnFwdArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace attn
+
+// ---------------------------------------------------------------------------
+// self-test of the bounded wait: one thread waits on an mbarrier phase that
+// nothing completes; the wait must give up after `timeout_ns`, record
+// ATTN_ERR_TIMEOUT in the status word and return.
+// ---------------------------------------------------------------------------
+namespace attn {
+namespace {
+__global__ void wait_timeout_selftest_kernel(uint32_t* status, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, status, timeout_ns);  // never arrives
+  __syncthreads();
+}
+}  // namespace
+
+cudaError_t launch_wait_timeout_selftest(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream) {
+  wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(status, timeout_ns);
+  return cudaGetLastError();
+}
+}  // namespace attn
