@@ -373,6 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_col = col_s(t);
     const uint32_t o_col = C::kColO0 + t * D;
+    // P as bf16 pairs (key 2i in the low half): its own region (D = 64) or the
+    // first 64 columns of S_t (D = 128)
+    const uint32_t p_col = C::kSepP ? C::kColP0 + t * 64 : s_col;
     const float* mbuf = reinterpret_cast<const float*>(smem + C::kOffMask);
     float m_run = -INFINITY;  // reference max, log2 units
     float l_run = 0.0f;       // running sum of 2^(x - m_run)
@@ -471,48 +474,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         float rsum[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) rsum[i] = 0.0f;
-        if (!masked_tile) {
-          const float neg = -m_sub;
+        auto chunk_out = [&](int c) {
+          uint32_t pw[16];
 #pragma unroll
-          for (int c = 0; c < kBN; ++c) {
-            const float pv = fast_exp2(fmaf(SV(c), prm.scale_log2, neg));
-            sr[c >> 5][c & 31] = __float_as_uint(pv);
-            rsum[c & 7] += pv;
-          }
-        } else {
+          for (int i = 0; i < 16; ++i)
+            pw[i] = pack_bf16x2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
+          tmem_st16(tmem + lane_addr + p_col + c * 16, pw);
+        };
+        // D = 128 stores P 32 keys at a time as they are exponentiated (each
+        // chunk's values die once in TMEM); D = 64 first exponentiates the whole
+        // row, giving PV_t(j-1) time to finish before it must wait for it
+        constexpr bool kChunked = !C::kSepP;
+        const float neg = -m_sub;
 #pragma unroll
-          for (int c = 0; c < kBN; ++c) {
-            const float pv = fast_exp2(SV(c) - m_sub);  // -inf -> 0
-            sr[c >> 5][c & 31] = __float_as_uint(pv);
-            rsum[c & 7] += pv;
+        for (int c = 0; c < 4; ++c) {
+          if (!masked_tile) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float pv = fast_exp2(fmaf(__uint_as_float(sr[c][i]), prm.scale_log2, neg));
+              sr[c][i] = __float_as_uint(pv);
+              rsum[i & 7] += pv;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const float pv = fast_exp2(__uint_as_float(sr[c][i]) - m_sub);  // -inf -> 0
+              sr[c][i] = __float_as_uint(pv);
+              rsum[i & 7] += pv;
+            }
           }
+          if constexpr (kChunked) chunk_out(c);
         }
         rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) + ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
+        if constexpr (!kChunked) {
+          // P_t and O_t are free once PV_t(j-1) has completed
+          if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], (j - 1) & 1, abort, prm.status))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 4; ++c) chunk_out(c);
+        }
+      } else {
+        // fast path passed its check: now P may overwrite S's columns
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pw[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pw[i] = pack_bf16x2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
+          tmem_st16(tmem + lane_addr + p_col + c * 16, pw);
+        }
       }
 #undef SV
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->m_empty[mb_i]);  // this warp is done with the mask tile
       l_run = l_run * alpha + rs;
 
-      if constexpr (C::kSepP) {
-        // P_t and O_t are free once PV_t(j-1) has completed
-        if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], (j - 1) & 1, abort, prm.status))) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-      }
-      // P as bf16 pairs (key 2i in the low half): its own region (D = 64) or
-      // the first 64 columns of S_t (D = 128)
-      const uint32_t p_col = C::kSepP ? C::kColP0 + t * 64 : s_col;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pw[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pw[i] = pack_bf16x2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
-        tmem_st16(tmem + lane_addr + p_col + c * 16, pw);
-      }
       // O_t is stable here: PV_t(j-1) has completed (o_done, or the commit
       // behind s_full when P shares S's columns)
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
