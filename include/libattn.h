@@ -212,9 +212,9 @@ attn_status paged_decode_attn(const attn_tensor *q, const attn_kv_cache *cache,
  *   call's status word: 0, or the bit (1 << ATTN_ERR_DEVICE_BOUNDS) when a
  *   block-table entry or context length was out of range.
  *   Returns ATTN_ERR_WORKSPACE when the call would need more than the 20 MiB
- *   scratch (batch * Hq * ceil(max_blocks*block_size/512) * (head_dim+1) * 4
+ *   scratch (batch * Hq * ceil(max_blocks*block_size/1024) * (head_dim+1) * 4
  *   bytes, plus 256); the 64-sequence, 32-head, head_dim 128 decode with
- *   contexts up to 8192 tokens needs 17.97 MB.
+ *   contexts up to 8192 tokens needs 9.51 MB.
  *   The first call on each device looks up the scratch array's device
  *   address (with that device current) and remembers it; make that first
  *   call before any stream capture.

@@ -6,7 +6,7 @@
 // The work is HBM-bound (about 4 flops per KV byte), so this is an FMA
 // kernel organised around the bytes:
 //  * split-K over the context: CTA (split s, KV head g, sequence b) covers
-//    tokens [512 s, 512 (s+1)) and all G = Hq/Hkv query heads of the group,
+//    tokens [1024 s, 1024 (s+1)) and all G = Hq/Hkv query heads of the group,
 //    so every K/V byte is read from HBM once;
 //  * each of the 4 warps walks every 4th 16-token block of the split; lane 0
 //    streams the block's K and V (4 KB each at D = 128) with 1-D bulk copies

@@ -26,7 +26,7 @@
 namespace {
 
 // 20 MiB: the 64-sequence, 32-head, D 128 decode with up to 8192-token
-// contexts (width 513 blocks) needs 17.97 MB including the status block.
+// contexts (width 513 blocks) needs 9.51 MB including the status block.
 constexpr size_t kNoAllocScratchBytes = size_t(20) << 20;
 constexpr int kMaxDevices = 64;
 

@@ -94,7 +94,7 @@ struct DecodeArgs {
   uint32_t* status;
 };
 // tokens per split-K work unit of the paged decode
-constexpr int kDecodeSplitTokens = 512;
+constexpr int kDecodeSplitTokens = 1024;
 int decode_num_splits(int max_blocks, int block_size);
 size_t decode_partial_bytes(int64_t B, int64_t Hq, int n_split, int D);
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);

@@ -59,9 +59,9 @@ def test_status_strings_and_version(L):
 def test_workspace_sizes(L):
     assert L.attn_fwd_workspace_size() == 256
     assert L.kv_append_workspace_size() == 256
-    # decode: status block + partials [B, Hq, n_split, D] + lse [B, Hq, n_split], split = 512 tokens
-    n_split = -(-513 * 16 // 512)
-    assert n_split == 17
+    # decode: status block + partials [B, Hq, n_split, D] + lse [B, Hq, n_split], split = 1024 tokens
+    n_split = -(-513 * 16 // 1024)
+    assert n_split == 9
     part = 64 * 32 * n_split * (128 + 1) * 4
     assert L.paged_decode_workspace_size(64, 32, 513, 16, 128) == 256 + (part + 255) // 256 * 256
     # linear in the longest context, never quadratic
