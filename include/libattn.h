@@ -122,6 +122,41 @@ attn_status attn_fwd(const attn_tensor *q, const attn_tensor *k, const attn_tens
                      void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * attn_fwd_varlen -- attn_fwd with the key padding given as lengths.
+ *
+ * The same attention as attn_fwd, where batch row b attends to its first
+ * key_lens[b] keys only (the padded tail of "MultiheadAttention fast path used
+ * 18 GB of VRAM": padding is a suffix of each sequence's patches).  This is
+ * exactly attn_fwd with an additive mask of 0 for keys < key_lens[b] and -inf
+ * after, but no mask is read and KV tiles past the length are skipped.
+ *   key_lens  int32 [B] device array; values are clamped to [0, Pk]; a row
+ *             with 0 keys gives out = 0 and lse = -inf.
+ * Other arguments, layouts and rules as attn_fwd.
+ */
+attn_status attn_fwd_varlen(const attn_tensor *q, const attn_tensor *k, const attn_tensor *v,
+                            const int32_t *key_lens, float scale,
+                            const attn_tensor *out, float *lse,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * attn_key_padding_to_additive -- turn a boolean key_padding_mask into the
+ * additive mask attn_fwd takes.
+ *
+ * "MultiheadAttention fast path used 18 GB of VRAM" (note on the mask
+ * direction): nn.MultiheadAttention's key_padding_mask marks a key to IGNORE
+ * with True, while SDPA's boolean attn_mask marks a key to KEEP with True;
+ * passing one as the other silently corrupts the result.  The library only
+ * takes the additive form; this converts the key_padding_mask convention:
+ *   additive_mask[b*out_stride_b + j] = key_padding_mask[b*kpm_stride_b + j] ? -inf : 0
+ *   key_padding_mask  uint8 [batch, num_keys] (non-zero = padded key), device
+ *   additive_mask     float32 [batch, num_keys], device, caller-owned
+ */
+attn_status attn_key_padding_to_additive(const uint8_t *key_padding_mask, int64_t kpm_stride_b,
+                                         int32_t batch, int64_t num_keys,
+                                         float *additive_mask, int64_t out_stride_b,
+                                         cudaStream_t stream);
+
+/*
  * attn_lse_merge -- combine n attention results computed over disjoint KV
  * chunks of the same queries.
  *

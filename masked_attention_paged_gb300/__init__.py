@@ -80,6 +80,8 @@ def load(build_if_missing: bool = False):
             "kv_append_workspace_size": (SZ, []),
             "paged_decode_workspace_size": (SZ, [I32, I32, I32, I32, I32]),
             "attn_fwd": (I32, [T, T, T, P, I64, F, T, P, P, SZ, P]),
+            "attn_fwd_varlen": (I32, [T, T, T, P, F, T, P, P, SZ, P]),
+            "attn_key_padding_to_additive": (I32, [P, I64, I32, I64, P, I64, P]),
             "attn_lse_merge": (I32, [I32, T, ctypes.POINTER(P), T, P, P]),
             "kv_append": (I32, [C, P, I64, I32, P, T, T, P, SZ, P]),
             "paged_decode_attn": (I32, [T, C, P, I64, I32, P, F, T, P, P, SZ, P]),
@@ -101,7 +103,8 @@ def exported_symbols() -> list[str]:
     return ["attn_fwd", "attn_lse_merge", "kv_append", "paged_decode_attn", "paged_kv_gather",
             "attn_fwd_workspace_size", "kv_append_workspace_size", "paged_decode_workspace_size",
             "attn_check_device_status", "attn_reset_device_status", "attn_status_string", "attn_version",
-            "paged_decode_attn_noalloc", "attn_selftest_wait_timeout"]
+            "paged_decode_attn_noalloc", "attn_selftest_wait_timeout", "attn_fwd_varlen",
+            "attn_key_padding_to_additive"]
 
 
 # --------------------------------------------------------------------------
@@ -221,6 +224,47 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, key_pad_mask: Op
                       ctypes.byref(do), _ptr(lse), ws.ptr, ws.nbytes, _stream(stream))
     _check("attn_fwd", st)
     return (out, lse) if return_lse else out
+
+
+def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, key_lens: torch.Tensor,
+                    scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                    lse: Optional[torch.Tensor] = None, return_lse: bool = True,
+                    workspace: Optional[Workspace] = None, stream=None):
+    """attn_fwd where batch row b attends to its first key_lens[b] keys (int32
+    [B] on the device); KV tiles past the length are skipped."""
+    lib = load()
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    assert key_lens.dtype == torch.int32 and key_lens.is_contiguous() and key_lens.is_cuda
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    ws = workspace or _small_ws(q.device)
+    dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
+    st = lib.attn_fwd_varlen(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), key_lens.data_ptr(), float(scale),
+                             ctypes.byref(do), _ptr(lse), ws.ptr, ws.nbytes, _stream(stream))
+    _check("attn_fwd_varlen", st)
+    return (out, lse) if return_lse else out
+
+
+def key_padding_to_additive(key_padding_mask: torch.Tensor, out: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    """Boolean [B, Pk] key_padding_mask (True = padded key, the
+    nn.MultiheadAttention convention) -> float32 additive mask (-inf / 0)."""
+    lib = load()
+    kpm = key_padding_mask
+    assert kpm.dim() == 2 and kpm.is_cuda and kpm.stride(1) == 1
+    if kpm.dtype == torch.bool:
+        kpm = kpm.view(torch.uint8)
+    assert kpm.dtype == torch.uint8
+    B, Pk = kpm.shape
+    if out is None:
+        out = torch.empty(B, Pk, dtype=torch.float32, device=kpm.device)
+    st = lib.attn_key_padding_to_additive(kpm.data_ptr(), kpm.stride(0), B, Pk, out.data_ptr(), out.stride(0),
+                                          _stream(stream))
+    _check("attn_key_padding_to_additive", st)
+    return out
 
 
 def attn_lse_merge(outs: Sequence[torch.Tensor], lses: Sequence[torch.Tensor], out: Optional[torch.Tensor] = None,

@@ -116,9 +116,10 @@ size_t paged_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t m
   return kStatusBytes + decode_partial_bytes(batch, num_q_heads, ns, head_dim);
 }
 
-attn_status attn_fwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v, const float* key_pad_mask,
-                     int64_t mask_stride_b, float scale, const attn_tensor* out, float* lse, void* workspace,
-                     size_t workspace_bytes, cudaStream_t stream) {
+static attn_status attn_fwd_impl(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                                 const float* key_pad_mask, int64_t mask_stride_b, const int32_t* key_lens,
+                                 float scale, const attn_tensor* out, float* lse, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
   attn_status st;
   if ((st = check_tensor(q, 4)) != ATTN_OK) return st;
   if ((st = check_tensor(k, 4)) != ATTN_OK) return st;
@@ -146,6 +147,7 @@ attn_status attn_fwd(const attn_tensor* q, const attn_tensor* k, const attn_tens
   a.q = view(q); a.k = view(k); a.v = view(v); a.out = view(out);
   a.mask = key_pad_mask;
   a.mask_stride = mask_stride_b;
+  a.key_lens = key_lens;
   a.scale = scale;
   a.lse = lse;
   a.status = static_cast<uint32_t*>(workspace);
@@ -159,6 +161,32 @@ attn_status attn_fwd(const attn_tensor* q, const attn_tensor* k, const attn_tens
   if (D > 128 || D % 4 != 0) return ATTN_ERR_UNSUPPORTED;
   if (!vec16_ok(q) || !vec16_ok(k) || !vec16_ok(v)) return ATTN_ERR_INVALID_ARG;
   return from_cuda(launch_attn_fwd_simt(a, stream));
+}
+
+attn_status attn_fwd(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v, const float* key_pad_mask,
+                     int64_t mask_stride_b, float scale, const attn_tensor* out, float* lse, void* workspace,
+                     size_t workspace_bytes, cudaStream_t stream) {
+  return attn_fwd_impl(q, k, v, key_pad_mask, mask_stride_b, nullptr, scale, out, lse, workspace, workspace_bytes,
+                       stream);
+}
+
+attn_status attn_fwd_varlen(const attn_tensor* q, const attn_tensor* k, const attn_tensor* v,
+                            const int32_t* key_lens, float scale, const attn_tensor* out, float* lse,
+                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (key_lens == nullptr) return ATTN_ERR_INVALID_ARG;
+  return attn_fwd_impl(q, k, v, nullptr, 0, key_lens, scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_key_padding_to_additive(const uint8_t* key_padding_mask, int64_t kpm_stride_b, int32_t batch,
+                                         int64_t num_keys, float* additive_mask, int64_t out_stride_b,
+                                         cudaStream_t stream) {
+  if (batch < 0 || num_keys < 0 || batch > 65535) return ATTN_ERR_INVALID_ARG;
+  if (batch == 0 || num_keys == 0) return ATTN_OK;
+  if (key_padding_mask == nullptr || additive_mask == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (batch > 1 && (kpm_stride_b < num_keys || out_stride_b < num_keys)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(additive_mask, 4)) return ATTN_ERR_INVALID_ARG;
+  return from_cuda(launch_padding_mask_to_additive(key_padding_mask, kpm_stride_b, batch, num_keys, additive_mask,
+                                                   out_stride_b, stream));
 }
 
 attn_status attn_lse_merge(int32_t n, const attn_tensor* outs, const float* const* lses, const attn_tensor* out,

@@ -30,6 +30,7 @@ struct SimtParams {
   int64_t qs[3], ks[3], vs[3];  // b, h, row strides (elements); dim stride 1
   const float* mask;
   int64_t mask_stride;
+  const int32_t* key_lens;  // per-batch valid keys, or null
   void* out;
   int64_t os[3];
   int out_bf16;
@@ -69,14 +70,19 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_simt_kernel(const SimtParam
   const float* vbase = p.v + b * p.vs[0] + g * p.vs[1];
   const float* mrow = p.mask ? p.mask + b * p.mask_stride : nullptr;
   const int vec_per_row = TPR * kSlice / 4;
+  int n_keys = p.Pk;  // keys of this batch row: all Pk, or its valid length
+  if (p.key_lens != nullptr) {
+    const int len = p.key_lens[b];
+    n_keys = len < 0 ? 0 : (len < p.Pk ? len : p.Pk);
+  }
 
-  for (int k0 = 0; k0 < p.Pk; k0 += kTileKeys) {
+  for (int k0 = 0; k0 < n_keys; k0 += kTileKeys) {
     __syncthreads();
     for (int i = threadIdx.x; i < kTileKeys * vec_per_row; i += kThreads) {
       const int key = i / vec_per_row;
       const int d = (i % vec_per_row) * 4;
       float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
-      if (k0 + key < p.Pk && d < p.D) {
+      if (k0 + key < n_keys && d < p.D) {
         kv = *reinterpret_cast<const float4*>(kbase + static_cast<int64_t>(k0 + key) * p.ks[2] + d);
         vv = *reinterpret_cast<const float4*>(vbase + static_cast<int64_t>(k0 + key) * p.vs[2] + d);
       }
@@ -86,7 +92,7 @@ __global__ void __launch_bounds__(kThreads) attn_fwd_simt_kernel(const SimtParam
     }
     if (threadIdx.x < kTileKeys) {
       const int key = k0 + threadIdx.x;
-      ms[threadIdx.x] = key < p.Pk ? (mrow ? mrow[key] * kLog2e : 0.f) : -INFINITY;
+      ms[threadIdx.x] = key < n_keys ? (mrow ? mrow[key] * kLog2e : 0.f) : -INFINITY;
     }
     __syncthreads();
 
@@ -181,6 +187,7 @@ cudaError_t launch_attn_fwd_simt(const AttnFwdArgs& a, cudaStream_t stream) {
   }
   p.mask = a.mask;
   p.mask_stride = a.mask_stride;
+  p.key_lens = a.key_lens;
   p.out = a.out.data;
   p.out_bf16 = a.out.dtype == ATTN_BF16;
   p.lse = a.lse;

@@ -103,11 +103,12 @@ struct TmaCoordMap {
 };
 
 struct TcParams {
-  int Pq, Pk, Hq, group, n_kv_tiles;
+  int Pq, Pk, Hq, group;
   float scale_log2;
   int scale_positive;  // max of raw scores == max of scaled scores
   const float* mask;
   int64_t mask_stride;
+  const int32_t* key_lens;  // per-batch valid keys, or null (all Pk)
   void* out;
   int64_t out_stride[3];  // b, h, row (elements)
   float* lse;
@@ -136,7 +137,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int b = blockIdx.z;
   const int g = h / prm.group;
   const int q0 = blockIdx.x * (2 * kBM);
-  const int nkv = prm.n_kv_tiles;
+  // keys of this batch row: all Pk, or its valid length (tiles past it are skipped)
+  int n_keys = prm.Pk;
+  if (prm.key_lens != nullptr) {
+    const int len = prm.key_lens[b];
+    n_keys = len < 0 ? 0 : (len < prm.Pk ? len : prm.Pk);
+  }
+  const int nkv = (n_keys + kBN - 1) / kBN;
   volatile int* abort = &bars->abort;
 
   if (threadIdx.x == 0) {
@@ -355,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int key = j * kBN + lane * 4 + e;
-        v[e] = key >= prm.Pk ? -INFINITY : (mrow ? mrow[key] * kLog2e : 0.0f);
+        v[e] = key >= n_keys ? -INFINITY : (mrow ? mrow[key] * kLog2e : 0.0f);
         any |= v[e] != 0.0f;
       }
       *reinterpret_cast<float4*>(mbuf + s * kBN + lane * 4) = make_float4(v[0], v[1], v[2], v[3]);
@@ -682,11 +689,11 @@ cudaError_t launch_tc(const AttnFwdArgs& a, cudaStream_t stream) {
   p.Pk = static_cast<int>(a.Pk);
   p.Hq = static_cast<int>(a.Hq);
   p.group = static_cast<int>(a.Hq / a.Hkv);
-  p.n_kv_tiles = static_cast<int>((a.Pk + kBN - 1) / kBN);
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   p.scale_positive = p.scale_log2 > 0.0f;
   p.mask = a.mask;
   p.mask_stride = a.mask_stride;
+  p.key_lens = a.key_lens;
   p.out = a.out.data;
   p.out_stride[0] = a.out.stride[0];
   p.out_stride[1] = a.out.stride[1];

@@ -21,6 +21,7 @@ struct AttnFwdArgs {
   View4 q, k, v, out;
   const float* mask;  // [B, Pk] additive, row stride mask_stride; may be null
   int64_t mask_stride;
+  const int32_t* key_lens;  // [B] valid keys per batch row (keys past it are padding); may be null
   float scale;
   float* lse;         // [B, Hq, Pq] contiguous, may be null
   uint32_t* status;   // device status word
@@ -98,6 +99,10 @@ constexpr int kDecodeSplitTokens = 1024;
 int decode_num_splits(int max_blocks, int block_size);
 size_t decode_partial_bytes(int64_t B, int64_t Hq, int n_split, int D);
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// boolean key-padding mask (non-zero = padded) -> additive 0 / -inf
+cudaError_t launch_padding_mask_to_additive(const uint8_t* kpm, int64_t kpm_stride, int64_t B, int64_t Pk,
+                                            float* out, int64_t out_stride, cudaStream_t stream);
 
 // one bounded mbarrier wait that nothing completes (exercises the timeout path)
 cudaError_t launch_wait_timeout_selftest(uint32_t* status, uint64_t timeout_ns, cudaStream_t stream);

@@ -338,3 +338,28 @@ cudaError_t launch_wait_timeout_selftest(uint32_t* status, uint64_t timeout_ns, 
   return cudaGetLastError();
 }
 }  // namespace attn
+
+// ---------------------------------------------------------------------------
+// boolean key-padding mask -> additive mask ("MultiheadAttention fast path
+// used 18 GB of VRAM", the note on mask direction: a key_padding_mask marks a
+// padded key with True, which must become -inf; 0 keeps the key)
+// ---------------------------------------------------------------------------
+namespace attn {
+namespace {
+__global__ void padding_mask_to_additive_kernel(const uint8_t* kpm, int64_t kpm_stride, int64_t Pk, float* out,
+                                                int64_t out_stride) {
+  const int64_t b = blockIdx.y;
+  for (int64_t j = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; j < Pk;
+       j += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    out[b * out_stride + j] = kpm[b * kpm_stride + j] ? -INFINITY : 0.0f;
+}
+}  // namespace
+
+cudaError_t launch_padding_mask_to_additive(const uint8_t* kpm, int64_t kpm_stride, int64_t B, int64_t Pk,
+                                            float* out, int64_t out_stride, cudaStream_t stream) {
+  const int64_t blocks = (Pk + 255) / 256;
+  dim3 grid(static_cast<unsigned>(blocks < 1024 ? blocks : 1024), static_cast<unsigned>(B));
+  padding_mask_to_additive_kernel<<<grid, 256, 0, stream>>>(kpm, kpm_stride, Pk, out, out_stride);
+  return cudaGetLastError();
+}
+}  // namespace attn

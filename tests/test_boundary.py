@@ -208,3 +208,27 @@ def test_paged_decode_rejects(L):
     assert call(mb=0) == INVALID
     assert call(q=_t([4, 32, 128], 0)) == UNSUPPORTED
     assert call(scale=float("inf")) == INVALID
+
+
+def test_attn_fwd_varlen_rejects(L):
+    q, k = _t(list(GOOD["q"])), _t(list(GOOD["k"]))
+    def call(kl=FAKE, ws=FAKE, qq=q):
+        return L.attn_fwd_varlen(ctypes.byref(qq), ctypes.byref(k), ctypes.byref(k), kl, 0.125, ctypes.byref(qq),
+                                 None, ws, 256, None)
+    assert call(kl=None) == INVALID
+    assert call(ws=None) == WORKSPACE
+    assert call(qq=_t([1, 4, 100, 128])) == INVALID  # head dim differs from k
+    assert call(qq=_t([1, 4, 0, 64])) == OK  # zero query rows: nothing launched
+
+
+def test_key_padding_converter_rejects(L):
+    def call(kpm=FAKE, ks=300, b=3, n=300, out=FAKE, os_=300):
+        return L.attn_key_padding_to_additive(kpm, ks, b, n, out, os_, None)
+    assert call(b=-1) == INVALID
+    assert call(n=-1) == INVALID
+    assert call(kpm=None) == INVALID
+    assert call(out=None) == INVALID
+    assert call(ks=299) == INVALID
+    assert call(os_=299) == INVALID
+    assert call(out=FAKE + 2) == INVALID  # float output must be 4-byte aligned
+    assert call(b=0) == OK and call(n=0) == OK
