@@ -20,6 +20,10 @@ Sources, by page title and section:
   token = layers x 2 x H_KV x D_head x B_elem.
 * decode -- "KV cache in nanoVLM" (how KV caching optimises inference): the
   new token's K/V is appended to the cache and its query attends over it.
+* prefill -- "KV cache in nanoVLM" (prefill and decode phases) and "LLM
+  inference memory accounting" (section 20, chunked prefill): a prompt or a
+  chunk of it is processed in one pass, its K/V written to the cache; a
+  causal query attends to no later position.
 
 Every function here is pinned by the ``-m "not gpu"`` tests in
 ``tests/test_oracle.py`` against brute force in arbitrary precision, a
@@ -74,6 +78,9 @@ def _load():
             lib.oracle_paged_decode.restype = ctypes.c_int
             lib.oracle_paged_decode.argtypes = [i64] * 6 + [p, ctypes.c_int, p, p, ctypes.c_int,
                                                            p, i64, i64, p, ctypes.c_double, p, p]
+            lib.oracle_paged_prefill.restype = ctypes.c_int
+            lib.oracle_paged_prefill.argtypes = [i64] * 7 + [p, ctypes.c_int, p, p, ctypes.c_int,
+                                                            p, i64, i64, p, ctypes.c_int, ctypes.c_double, p, p]
             lib.oracle_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -212,6 +219,28 @@ def kv_append(k_cache, v_cache, block_table, pos, k_new, v_new, block_size: int 
     return kc, vc
 
 
+def kv_append_chunk(k_cache, v_cache, block_table, start_pos, k_new, v_new, block_size: int = 16):
+    """Expected caches after appending a chunk of T tokens per sequence.
+
+    Token i of sequence b's chunk (``k_new[b, :, i]``, ``[B, Hkv, T, D]``) goes
+    to position ``start_pos[b] + i``: physical block
+    ``block_table[b, (start_pos[b] + i) // block_size]``, slot
+    ``(start_pos[b] + i) % block_size``.  Bit patterns, like ``kv_append``."""
+    kc = _bits(k_cache).copy()
+    vc = _bits(v_cache).copy()
+    bt = np.asarray(_np(block_table), dtype=np.int64)
+    sp = np.asarray(_np(start_pos), dtype=np.int64)
+    kn = _bits(k_new)
+    vn = _bits(v_new)
+    for b in range(sp.shape[0]):
+        for i in range(kn.shape[2]):
+            t = sp[b] + i
+            blk = bt[b, t // block_size]
+            kc[blk, :, t % block_size, :] = kn[b, :, i, :]
+            vc[blk, :, t % block_size, :] = vn[b, :, i, :]
+    return kc, vc
+
+
 def paged_gather(cache, block_table, lens, block_size: int = 16):
     """Contiguous per-sequence K (or V) by walking the block table token by
     token: result[b] has shape [Hkv, lens[b], D] (raw integer bit patterns)."""
@@ -245,6 +274,7 @@ def paged_decode(q, k_cache, v_cache, block_table, ctx_lens, scale: Optional[flo
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     qa, qc = _as_host(q.contiguous() if hasattr(q, "contiguous") else q)
+    qa = qa.contiguous()  # held here: the C call reads it
     ka, kc = _as_host(k_cache.contiguous())
     va, vc = _as_host(v_cache.contiguous())
     assert kc == vc
@@ -252,13 +282,49 @@ def paged_decode(q, k_cache, v_cache, block_table, ctx_lens, scale: Optional[flo
     cl = torch.as_tensor(_np(ctx_lens)).to(torch.int32).contiguous()
     out = np.zeros((B, Hq, D), dtype=np.float64)
     lse = np.zeros((B, Hq), dtype=np.float64)
-    rc = lib.oracle_paged_decode(B, Hq, Hkv, D, bs, nb, qa.contiguous().data_ptr(), qc,
+    rc = lib.oracle_paged_decode(B, Hq, Hkv, D, bs, nb, qa.data_ptr(), qc,
                                  ka.data_ptr(), va.data_ptr(), kc,
                                  bt.data_ptr(), bt.stride(0), bt.shape[1], cl.data_ptr(),
                                  float(scale), out.ctypes.data, lse.ctypes.data)
     if rc != 0:
         raise ValueError("oracle_paged_decode: block table entry outside the cache "
                          "or context longer than the table")
+    return out, lse
+
+
+def paged_prefill(q, k_cache, v_cache, block_table, start_pos, causal: bool, scale: Optional[float] = None,
+                  block_size: int = 16):
+    """A chunk of T query tokens per sequence attending over its paged cache.
+
+    q: [B, Hq, T, D]; caches [num_blocks, Hkv, block_size, D] that already
+    hold the chunk at positions ``start_pos[b] + i``; block_table int32
+    [B, width]; start_pos int32 [B] (tokens cached before the chunk).  Query
+    i attends over positions ``[0, start_pos[b] + i]`` when ``causal``, else
+    over ``[0, start_pos[b] + T)``.  Returns float64 (out [B, Hq, T, D],
+    lse [B, Hq, T])."""
+    import torch
+    lib = _load()
+    B, Hq, T, D = q.shape
+    nb, Hkv, bs, Dk = k_cache.shape
+    assert bs == block_size and Dk == D
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    qa, qc = _as_host(q.contiguous() if hasattr(q, "contiguous") else q)
+    qa = qa.contiguous()  # held here: the C call reads it
+    ka, kc = _as_host(k_cache.contiguous())
+    va, vc = _as_host(v_cache.contiguous())
+    assert kc == vc
+    bt = torch.as_tensor(_np(block_table)).to(torch.int32).contiguous()
+    sp = torch.as_tensor(_np(start_pos)).to(torch.int32).contiguous()
+    out = np.zeros((B, Hq, T, D), dtype=np.float64)
+    lse = np.zeros((B, Hq, T), dtype=np.float64)
+    rc = lib.oracle_paged_prefill(B, Hq, Hkv, T, D, bs, nb, qa.data_ptr(), qc,
+                                  ka.data_ptr(), va.data_ptr(), kc,
+                                  bt.data_ptr(), bt.stride(0), bt.shape[1], sp.data_ptr(), int(bool(causal)),
+                                  float(scale), out.ctypes.data, lse.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_paged_prefill: block table entry outside the cache "
+                         "or sequence longer than the table")
     return out, lse
 
 

@@ -22,6 +22,10 @@
  *    token t sits in logical block t / block_size at slot t % block_size.
  *  - Decode, "KV cache in nanoVLM" (incremental computation): one query token
  *    per sequence attends over every cached key, the new one included.
+ *  - Prefill, "KV cache in nanoVLM" (prefill and decode phases) and "LLM
+ *    inference memory accounting" (section 20, chunked prefill): a prompt, or
+ *    a chunk of it, is processed in one pass; its tokens' K/V join the cache
+ *    and each of its queries attends over the cache.
  *
  * Readings where the pages are silent:
  *  - A row whose keys are all masked has no softmax; the oracle returns
@@ -188,6 +192,54 @@ int oracle_paged_decode(int64_t B, int64_t Hq, int64_t Hkv, int64_t D, int64_t b
             for (int64_t d = 0; d < D; ++d) qv[d] = widen(q, q_dtype, (b * Hq + h) * D + d);
             attend_row(L, D, scale, qv, k_cache, v_cache, kv_dtype, ki, ki, NULL, s,
                        out + bh * D, lse + bh);
+        }
+        free(s); free(qv); free(ki);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Paged prefill of a chunk of T new tokens per sequence.  Sequence b already
+ * held start_pos[b] tokens; token i of its chunk sits at position
+ * start_pos[b] + i, and the caches passed here already contain the chunk.
+ * Query i of (b, h) attends over the tokens [0, n) of KV head h / (Hq / Hkv),
+ * each read through the block table like the decode above, with
+ *   n = start_pos[b] + i + 1   when causal (no token after its own position)
+ *   n = start_pos[b] + T       otherwise (every token of the chunk).
+ * q: [B, Hq, T, D] contiguous.  out: [B, Hq, T, D], lse: [B, Hq, T].
+ * Returns 0, or -1 if a table entry points outside the cache or a sequence
+ * needs more blocks than max_blocks.
+ */
+int oracle_paged_prefill(int64_t B, int64_t Hq, int64_t Hkv, int64_t T, int64_t D, int64_t block_size,
+                         int64_t num_blocks, const void *q, int q_dtype,
+                         const void *k_cache, const void *v_cache, int kv_dtype,
+                         const int32_t *block_table, int64_t bt_stride, int64_t max_blocks,
+                         const int32_t *start_pos, int causal, double scale, double *out, double *lse) {
+    if (Hkv <= 0 || Hq % Hkv != 0) return -1;
+    const int64_t group = Hq / Hkv;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < B * Hq * T; ++r) {
+        int64_t i = r % T, h = (r / T) % Hq, b = r / (T * Hq);
+        int64_t g = h / group;
+        int64_t start = start_pos[b];
+        int64_t total = start + T;
+        if (start < 0 || (total + block_size - 1) / block_size > max_blocks) { bad = 1; continue; }
+        int64_t n = causal ? start + i + 1 : total;
+        double *s = (double *)malloc(sizeof(double) * (size_t)n);
+        double *qv = (double *)malloc(sizeof(double) * (size_t)D);
+        int64_t *ki = (int64_t *)malloc(sizeof(int64_t) * (size_t)n);
+        int ok = 1;
+        for (int64_t t = 0; t < n; ++t) {
+            int64_t blk = block_table[b * bt_stride + t / block_size];
+            if (blk < 0 || blk >= num_blocks) { ok = 0; break; }
+            ki[t] = ((blk * Hkv + g) * block_size + t % block_size) * D;
+        }
+        if (!ok) {
+            bad = 1;
+        } else {
+            for (int64_t d = 0; d < D; ++d) qv[d] = widen(q, q_dtype, r * D + d);
+            attend_row(n, D, scale, qv, k_cache, v_cache, kv_dtype, ki, ki, NULL, s, out + r * D, lse + r);
         }
         free(s); free(qv); free(ki);
     }

@@ -271,3 +271,105 @@ def decode_kv_bytes(ctx_lens: torch.Tensor, Hkv: int, D: int, elem_bytes: int = 
     """Algorithmic KV bytes one decode step reads: K and V of every attended
     token of every KV head."""
     return int(ctx_lens.to(torch.int64).sum().item()) * 2 * Hkv * D * elem_bytes
+
+
+# --------------------------------------------------------------------------
+# Paged (chunked) prefill
+# --------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class PrefillConfig:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    T: int  # chunk tokens per sequence
+    block_size: int
+    start_lo: int  # tokens cached before the chunk, inclusive range
+    start_hi: int
+    spare_blocks: int
+    causal: bool = True
+    scale: Optional[float] = None
+
+    @property
+    def softmax_scale(self) -> float:
+        return self.scale if self.scale is not None else 1.0 / math.sqrt(self.D)
+
+
+PREFILL_CONFIGS = {
+    # the decode workload's model shape (32 query heads on 8 KV heads, D 128,
+    # 16-token blocks); 16 sequences each prefilling a 1024-token chunk after
+    # 0..7168 cached tokens
+    "prefill_chunk": PrefillConfig("prefill_chunk", 16, 32, 8, 128, 1024, 16, 0, 7168, 16),
+}
+
+
+@dataclasses.dataclass
+class PrefillInputs:
+    cfg: PrefillConfig
+    start_pos: torch.Tensor  # int32 [B]: tokens cached before the chunk
+    block_table: torch.Tensor  # int32 [B, width]; unused entries are -1
+    k_cache: torch.Tensor  # [num_blocks, Hkv, block_size, D]; NaN where nothing is cached
+    v_cache: torch.Tensor
+    k_new: torch.Tensor  # [B, Hkv, T, D]: the chunk's keys and values
+    v_new: torch.Tensor
+    q: torch.Tensor  # [B, Hq, T, D]
+    scale: float
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.k_cache.shape[0])
+
+    @property
+    def max_blocks(self) -> int:
+        return int(self.block_table.shape[1])
+
+
+def make_prefill_inputs(cfg: PrefillConfig, seed: int = 0, start: Optional[Sequence[int]] = None,
+                        dtype: torch.dtype = torch.bfloat16) -> PrefillInputs:
+    """Paged-cache prefill inputs: ``start`` (drawn uniform in
+    ``[start_lo, start_hi]`` unless given) tokens are cached per sequence and
+    a chunk of ``T`` follows.  Each sequence owns ``ceil((start + T) /
+    block_size)`` physical blocks from one seeded random permutation;
+    unfilled slots hold NaN, so reading one shows."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    B, bs, T = cfg.B, cfg.block_size, cfg.T
+    if start is None:
+        st = torch.randint(cfg.start_lo, cfg.start_hi + 1, (B,), generator=g)
+    else:
+        st = torch.tensor(list(start), dtype=torch.int64)
+        assert st.numel() == B
+    total = st + T
+    nblk = (total + bs - 1) // bs
+    width = int(nblk.max().item()) if B > 0 else 1
+    n_phys = int(nblk.sum().item()) + cfg.spare_blocks
+    perm = torch.randperm(n_phys, generator=g)
+    bt = torch.full((B, max(width, 1)), -1, dtype=torch.int32)
+    off = 0
+    for b in range(B):
+        n = int(nblk[b])
+        bt[b, :n] = perm[off:off + n].to(torch.int32)
+        off += n
+    k_cache = _randn((n_phys, cfg.Hkv, bs, cfg.D), g, dtype)
+    v_cache = _randn((n_phys, cfg.Hkv, bs, cfg.D), g, dtype)
+    filled = torch.zeros(n_phys, bs, dtype=torch.bool)
+    for b in range(B):
+        t = torch.arange(int(st[b]))
+        filled[bt[b, (t // bs)].long(), t % bs] = True
+    k_cache.permute(0, 2, 1, 3)[~filled] = float("nan")
+    v_cache.permute(0, 2, 1, 3)[~filled] = float("nan")
+    k_new = _randn((B, cfg.Hkv, T, cfg.D), g, dtype)
+    v_new = _randn((B, cfg.Hkv, T, cfg.D), g, dtype)
+    q = _randn((B, cfg.Hq, T, cfg.D), g, dtype)
+    return PrefillInputs(cfg, st.to(torch.int32), bt, k_cache, v_cache, k_new, v_new, q, cfg.softmax_scale)
+
+
+def prefill_flops(start_pos: torch.Tensor, T: int, Hq: int, D: int, causal: bool) -> float:
+    """Algorithmic FLOPs of a prefill chunk: 4*D per (query, attended key)
+    per head; query i of a causal chunk attends start + i + 1 keys."""
+    st = start_pos.to(torch.float64)
+    if causal:
+        keys = (st * T + T * (T + 1) / 2).sum().item()
+    else:
+        keys = ((st + T) * T).sum().item()
+    return 4.0 * Hq * D * keys
