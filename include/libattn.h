@@ -230,6 +230,31 @@ attn_status paged_decode_attn(const attn_tensor *q, const attn_kv_cache *cache,
                               void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * paged_decode_attn_append -- kv_append and paged_decode_attn in one launch
+ * ("KV cache in nanoVLM": each decode step computes the newest token's K/V,
+ * adds it to the cache and attends with its query over the whole cache).
+ *
+ * The result equals kv_append(cache, block_table, pos, k_new, v_new) followed
+ * by paged_decode_attn with ctx_lens[b] = pos[b] + 1, bit for bit in the
+ * cache: the new token is written to block block_table[b][pos[b]/block_size],
+ * slot pos[b] % block_size, and every query attends over tokens [0, pos[b]].
+ * pos[b] < 0 leaves the cache alone and gives out = 0, lse = -inf.  A
+ * position past the table or a bad block id sets ATTN_ERR_DEVICE_BOUNDS.
+ *
+ *   q            [batch, Hq, head_dim] bf16
+ *   k_new, v_new [batch, Hkv, head_dim] bf16 (strided views)
+ *   pos          int32 [batch]: the new token's position (tokens cached before it)
+ *   workspace    as paged_decode_attn, same size for the same max_blocks
+ * The appended slot must not be read by another sequence of the same call
+ * (blocks shared between sequences are never appended to).
+ */
+attn_status paged_decode_attn_append(const attn_tensor *q, const attn_tensor *k_new, const attn_tensor *v_new,
+                                     const attn_kv_cache *cache, const int32_t *block_table,
+                                     int64_t bt_stride, int32_t max_blocks, const int32_t *pos,
+                                     float scale, const attn_tensor *out, float *lse,
+                                     void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * paged_decode_attn_noalloc -- the same paged decode for callers that cannot
  * allocate device memory.  The pages have no counterpart to this call; it
  * exists for this library's users.

@@ -85,6 +85,7 @@ def load(build_if_missing: bool = False):
             "attn_lse_merge": (I32, [I32, T, ctypes.POINTER(P), T, P, P]),
             "kv_append": (I32, [C, P, I64, I32, P, T, T, P, SZ, P]),
             "paged_decode_attn": (I32, [T, C, P, I64, I32, P, F, T, P, P, SZ, P]),
+            "paged_decode_attn_append": (I32, [T, T, T, C, P, I64, I32, P, F, T, P, P, SZ, P]),
             "paged_kv_gather": (I32, [C, I32, P, I64, I32, P, I32, I64, P, P, SZ, P]),
             "paged_decode_attn_noalloc": (I32, [T, C, P, I64, I32, P, F, T, P, P, P]),
             "attn_check_device_status": (I32, [P, ctypes.POINTER(ctypes.c_uint32), P]),
@@ -104,7 +105,7 @@ def exported_symbols() -> list[str]:
             "attn_fwd_workspace_size", "kv_append_workspace_size", "paged_decode_workspace_size",
             "attn_check_device_status", "attn_reset_device_status", "attn_status_string", "attn_version",
             "paged_decode_attn_noalloc", "attn_selftest_wait_timeout", "attn_fwd_varlen",
-            "attn_key_padding_to_additive"]
+            "attn_key_padding_to_additive", "paged_decode_attn_append"]
 
 
 # --------------------------------------------------------------------------
@@ -341,6 +342,38 @@ def paged_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
                                max_blocks, ctx_lens.data_ptr(), float(scale), ctypes.byref(do), _ptr(lse),
                                ws.ptr, ws.nbytes, _stream(stream))
     _check("paged_decode_attn", st)
+    return (out, lse) if return_lse else out
+
+
+def paged_decode_attn_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                             v_cache: torch.Tensor, block_table: torch.Tensor, pos: torch.Tensor,
+                             scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                             lse: Optional[torch.Tensor] = None, return_lse: bool = False,
+                             workspace: Optional[Workspace] = None, stream=None):
+    """kv_append(pos, k_new, v_new) and the decode over tokens [0, pos[b]] in
+    one launch; k_new, v_new [B, Hkv, D], pos int32 [B]."""
+    lib = load()
+    B, Hq, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1
+    assert pos.dtype == torch.int32 and pos.is_contiguous()
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    max_blocks = block_table.shape[1]
+    need = paged_decode_workspace_size(B, Hq, max_blocks, k_cache.shape[2], D)
+    ws = workspace
+    if ws is None or ws.nbytes < need:
+        ws = Workspace(need, device=q.device)
+    c = _cache(k_cache, v_cache)
+    dq, dk, dv, do = _desc(q), _desc(k_new), _desc(v_new), _desc(out)
+    st = lib.paged_decode_attn_append(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), ctypes.byref(c),
+                                      block_table.data_ptr(), block_table.stride(0), max_blocks, pos.data_ptr(),
+                                      float(scale), ctypes.byref(do), _ptr(lse), ws.ptr, ws.nbytes,
+                                      _stream(stream))
+    _check("paged_decode_attn_append", st)
     return (out, lse) if return_lse else out
 
 

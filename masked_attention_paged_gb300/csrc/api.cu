@@ -281,10 +281,12 @@ attn_status paged_kv_gather(const attn_kv_cache* cache, int32_t which, const int
   return from_cuda(launch_paged_gather(a, stream));
 }
 
-attn_status paged_decode_attn(const attn_tensor* q, const attn_kv_cache* cache, const int32_t* block_table,
-                              int64_t bt_stride, int32_t max_blocks, const int32_t* ctx_lens, float scale,
-                              const attn_tensor* out, float* lse, void* workspace, size_t workspace_bytes,
-                              cudaStream_t stream) {
+static attn_status paged_decode_impl(const attn_tensor* q, const attn_tensor* k_new, const attn_tensor* v_new,
+                                     const attn_kv_cache* cache, const int32_t* block_table, int64_t bt_stride,
+                                     int32_t max_blocks, const int32_t* lens_or_pos, float scale,
+                                     const attn_tensor* out, float* lse, void* workspace, size_t workspace_bytes,
+                                     cudaStream_t stream) {
+  const int32_t* ctx_lens = lens_or_pos;
   attn_status st;
   if ((st = check_cache(cache)) != ATTN_OK) return st;
   if ((st = check_tensor(q, 3)) != ATTN_OK) return st;
@@ -310,9 +312,22 @@ attn_status paged_decode_attn(const attn_tensor* q, const attn_kv_cache* cache, 
   if (!aligned(out->data, 8)) return ATTN_ERR_INVALID_ARG;
   for (int i = 0; i < 2; ++i)
     if (out->stride[i] % 2 != 0 && out->shape[i] > 1) return ATTN_ERR_INVALID_ARG;
+  const bool fused = k_new != nullptr || v_new != nullptr;
+  if (fused) {
+    if ((st = check_tensor(k_new, 3)) != ATTN_OK) return st;
+    if ((st = check_tensor(v_new, 3)) != ATTN_OK) return st;
+    if (k_new->dtype != ATTN_BF16 || v_new->dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+    for (int i = 0; i < 3; ++i)
+      if (v_new->shape[i] != k_new->shape[i]) return ATTN_ERR_INVALID_ARG;
+    if (k_new->shape[0] != B || k_new->shape[1] != cache->num_kv_heads || k_new->shape[2] != D)
+      return ATTN_ERR_INVALID_ARG;
+    if (!vec16_ok(k_new) || !vec16_ok(v_new)) return ATTN_ERR_INVALID_ARG;
+  }
   DecodeArgs a;
   a.cache = paged(cache);
   a.q = view(q);
+  a.k_new = fused ? view(k_new) : View4{};
+  a.v_new = fused ? view(v_new) : View4{};
   a.out = view(out);
   a.lse = lse;
   a.block_table = block_table;
@@ -326,6 +341,23 @@ attn_status paged_decode_attn(const attn_tensor* q, const attn_kv_cache* cache, 
   a.n_split = decode_num_splits(max_blocks, cache->block_size);
   a.status = static_cast<uint32_t*>(workspace);
   return from_cuda(launch_paged_decode(a, stream));
+}
+
+attn_status paged_decode_attn(const attn_tensor* q, const attn_kv_cache* cache, const int32_t* block_table,
+                              int64_t bt_stride, int32_t max_blocks, const int32_t* ctx_lens, float scale,
+                              const attn_tensor* out, float* lse, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
+  return paged_decode_impl(q, nullptr, nullptr, cache, block_table, bt_stride, max_blocks, ctx_lens, scale, out,
+                           lse, workspace, workspace_bytes, stream);
+}
+
+attn_status paged_decode_attn_append(const attn_tensor* q, const attn_tensor* k_new, const attn_tensor* v_new,
+                                     const attn_kv_cache* cache, const int32_t* block_table, int64_t bt_stride,
+                                     int32_t max_blocks, const int32_t* pos, float scale, const attn_tensor* out,
+                                     float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (k_new == nullptr || v_new == nullptr) return ATTN_ERR_INVALID_ARG;
+  return paged_decode_impl(q, k_new, v_new, cache, block_table, bt_stride, max_blocks, pos, scale, out, lse,
+                           workspace, workspace_bytes, stream);
 }
 
 attn_status attn_selftest_wait_timeout(void* workspace, size_t workspace_bytes, uint32_t timeout_us,

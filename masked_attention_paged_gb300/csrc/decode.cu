@@ -17,6 +17,11 @@
 //    softmax keeps per-head running max/sum in log2 units with lazy rescale;
 //  * the split's (output, LSE) goes to the workspace and a second kernel
 //    merges the splits with the LSE rule of the ring-attention page.
+// Fused append ("KV cache in nanoVLM": compute the new token's K/V, add it to
+// the cache, attend): ctx_lens then holds each sequence's new-token position
+// and the token itself is handed in.  Only the CTA whose split ends at that
+// position reads its slot, so it substitutes the new K/V row into its copy of
+// the block once the block has landed, and writes the row to the cache.
 #include <math.h>
 
 #include "common.cuh"
@@ -53,6 +58,10 @@ struct DecodeParams {
   int64_t bt_stride;
   int max_blocks;
   const int32_t* ctx_lens;
+  int len_add;  // 1 with a fused append: ctx_lens holds the new token's position
+  const uint16_t* k_new;  // fused append: [B, Hkv, D] rows (null otherwise)
+  const uint16_t* v_new;
+  int64_t kn_stride[2], vn_stride[2];  // batch, head
   float scale_log2;
   float* o_part;    // [B, Hq, n_split, D]
   float* lse_part;  // [B, Hq, n_split], log2 units
@@ -85,8 +94,8 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeP
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int cl = lane % Gm::CPR;  // chunk column
   const int ts = lane / Gm::CPR;  // token set
-  int L = p.ctx_lens[b];
-  if (L < 0) L = 0;
+  const int L_req = p.ctx_lens[b] + p.len_add;
+  int L = L_req < 0 ? 0 : L_req;
   if (L > p.max_blocks * kBS) {
     if (threadIdx.x == 0 && split == 0) report(p.status, kStatusBounds);
     L = p.max_blocks * kBS;
@@ -96,6 +105,13 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeP
   const int t_end = min(L, t_begin + kDecodeSplitTokens);
   const int nblk = (t_end - t_begin + kBS - 1) / kBS;
   const int lb0 = t_begin / kBS;
+  // fused append: the new token is the last of the context (when it fits the
+  // table); i_new is this warp's iteration over its block, or -1
+  int i_new = -1;
+  if (p.k_new != nullptr && L_req >= 1 && L_req == L && L - 1 >= t_begin) {
+    const int rel = (L - 1) / kBS - lb0;
+    if (rel % kWarps == warp) i_new = rel / kWarps;
+  }
 
   uint8_t* wbuf = smem + warp * kStages * 2 * Gm::BLOCK_BYTES;
   uint64_t* wbar = bars + warp * kStages;
@@ -178,8 +194,26 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeP
       break;
     }
     if (blk >= 0) {
-      const uint8_t* kb = wbuf + s * 2 * Gm::BLOCK_BYTES;
-      const uint8_t* vb = kb + Gm::BLOCK_BYTES;
+      uint8_t* kb = wbuf + s * 2 * Gm::BLOCK_BYTES;
+      uint8_t* vb = kb + Gm::BLOCK_BYTES;
+      if (i == i_new) {
+        // the block has landed: put the new token's row in place of whatever
+        // the slot held, and store it to the cache (lanes [0, CPR) carry K's
+        // 16-byte chunks, lanes [CPR, 2 CPR) V's)
+        const int slot = (L - 1) % kBS;
+        if (lane < 2 * Gm::CPR) {
+          const bool is_v = lane >= Gm::CPR;
+          const int c = lane % Gm::CPR;
+          const uint16_t* src = is_v ? p.v_new + b * p.vn_stride[0] + g * p.vn_stride[1]
+                                     : p.k_new + b * p.kn_stride[0] + g * p.kn_stride[1];
+          const uint4 w = *reinterpret_cast<const uint4*>(src + c * 8);
+          *reinterpret_cast<uint4*>((is_v ? vb : kb) + slot * (D * 2) + c * 16) = w;
+          uint16_t* cache = const_cast<uint16_t*>(is_v ? p.vc : p.kc);
+          const int64_t off = (static_cast<int64_t>(blk) * p.Hkv + g) * (kBS * D) + slot * D + c * 8;
+          *reinterpret_cast<uint4*>(cache + off) = w;
+        }
+        __syncwarp();
+      }
       const int tok0 = (lb0 + warp + kWarps * i) * kBS;  // first token of the block
 
       // partial dot products over this lane's 8 dims
@@ -349,7 +383,7 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeP
 // page, with the LSEs in log2 units.  One warp per (sequence, head).
 template <int D>
 __global__ void decode_reduce_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
-                                     const int32_t* __restrict__ ctx_lens, int max_tokens, int n_split,
+                                     const int32_t* __restrict__ ctx_lens, int len_add, int max_tokens, int n_split,
                                      int64_t B, int Hq, void* out, int out_bf16, int64_t os0, int64_t os1,
                                      float* lse) {
   constexpr int DPL = D / 32;  // dims per lane
@@ -358,7 +392,7 @@ __global__ void decode_reduce_kernel(const float* __restrict__ o_part, const flo
   if (wid >= B * Hq) return;
   const int64_t b = wid / Hq;
   const int h = static_cast<int>(wid % Hq);
-  int L = ctx_lens[b];
+  int L = ctx_lens[b] + len_add;
   L = L < 0 ? 0 : (L > max_tokens ? max_tokens : L);
   const int ns = (L + kDecodeSplitTokens - 1) / kDecodeSplitTokens;
   const int64_t base = wid * n_split;
@@ -409,7 +443,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodeParams& p, cudaStream
   if (e != cudaSuccess) return e;
   const int64_t warps = a.B * a.Hq;
   const unsigned blocks = static_cast<unsigned>((warps * 32 + 127) / 128);
-  decode_reduce_kernel<D><<<blocks, 128, 0, stream>>>(p.o_part, p.lse_part, a.ctx_lens, a.max_blocks * kBS,
+  decode_reduce_kernel<D><<<blocks, 128, 0, stream>>>(p.o_part, p.lse_part, a.ctx_lens, p.len_add, a.max_blocks * kBS,
                                                      a.n_split, a.B, static_cast<int>(a.Hq), a.out.data,
                                                      a.out.dtype == ATTN_BF16, a.out.stride[0], a.out.stride[1],
                                                      a.lse);
@@ -442,6 +476,13 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.bt_stride = a.bt_stride;
   p.max_blocks = a.max_blocks;
   p.ctx_lens = a.ctx_lens;
+  p.len_add = a.k_new.data != nullptr ? 1 : 0;
+  p.k_new = static_cast<const uint16_t*>(a.k_new.data);
+  p.v_new = static_cast<const uint16_t*>(a.v_new.data);
+  p.kn_stride[0] = a.k_new.stride[0];
+  p.kn_stride[1] = a.k_new.stride[1];
+  p.vn_stride[0] = a.v_new.stride[0];
+  p.vn_stride[1] = a.v_new.stride[1];
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   const size_t n = static_cast<size_t>(a.B) * a.Hq * a.n_split;
   p.o_part = static_cast<float*>(a.partials);

@@ -87,7 +87,8 @@ struct DecodeArgs {
   const int32_t* block_table;
   int64_t bt_stride;
   int max_blocks;
-  const int32_t* ctx_lens;
+  const int32_t* ctx_lens;  // or, with k_new set, each sequence's new-token position
+  View4 k_new, v_new;       // fused append: [B, Hkv, D]; data null for a plain decode
   int64_t B, Hq;
   float scale;
   void* partials;  // workspace after the status block

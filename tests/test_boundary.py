@@ -232,3 +232,19 @@ def test_key_padding_converter_rejects(L):
     assert call(os_=299) == INVALID
     assert call(out=FAKE + 2) == INVALID  # float output must be 4-byte aligned
     assert call(b=0) == OK and call(n=0) == OK
+
+
+def test_fused_decode_rejects(L):
+    need = L.paged_decode_workspace_size(4, 32, 10, 16, 128)
+    kn = _t([4, 8, 128])
+    def call(k=kn, v=kn, ws_bytes=need):
+        q, out, c = _t([4, 32, 128]), _t([4, 32, 128]), _cache()
+        return L.paged_decode_attn_append(ctypes.byref(q), None if k is None else ctypes.byref(k),
+                                          None if v is None else ctypes.byref(v), ctypes.byref(c), FAKE, 10, 10,
+                                          FAKE, 0.1, ctypes.byref(out), None, FAKE, ws_bytes, None)
+    assert call(k=None) == INVALID
+    assert call(v=None) == INVALID
+    assert call(k=_t([4, 4, 128])) == INVALID  # heads differ from the cache
+    assert call(v=_t([4, 8, 128], 0)) == INVALID  # f32
+    assert call(k=_t([3, 8, 128]), v=_t([3, 8, 128])) == INVALID  # batch differs from q
+    assert call(ws_bytes=need - 256) == WORKSPACE

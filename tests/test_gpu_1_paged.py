@@ -178,3 +178,68 @@ def test_incremental_decode_equals_recompute_on_gpu():
         diff = (o2[0, :, 0].float() - out[b].float()).abs().max().item()
         assert diff <= 2e-2
         assert (l2[0, :, 0] - lse[b]).abs().max().item() <= 1e-3
+
+
+def _fused_and_check(d: workloads.DecodeInputs, note=""):
+    """paged_decode_attn_append against the oracle's kv_append then decode:
+    the cache bit for bit, the outputs within the bf16 tolerances."""
+    g = _dev(d)
+    ws = lib.Workspace(lib.paged_decode_workspace_size(d.cfg.B, d.cfg.Hq, d.block_table.shape[1], 16, d.cfg.D))
+    out, lse = lib.paged_decode_attn_append(g["q"], g["k_new"], g["v_new"], g["k_cache"], g["v_cache"],
+                                            g["block_table"], g["pos"], d.scale, return_lse=True, workspace=ws)
+    assert ws.status() == 0
+    ek, ev = oracle.kv_append(d.k_cache, d.v_cache, d.block_table, d.pos, d.k_new, d.v_new)
+    assert np.array_equal(g["k_cache"].cpu().view(torch.int16).numpy(), ek)
+    assert np.array_equal(g["v_cache"].cpu().view(torch.int16).numpy(), ev)
+    ro, rl = oracle.paged_decode(d.q, torch.from_numpy(ek).view(torch.bfloat16),
+                                 torch.from_numpy(ev).view(torch.bfloat16), d.block_table, d.ctx_lens, d.scale)
+    assert_out_close(out, ro, what="fused decode out" + note)
+    assert_lse_close(lse, rl, what="fused decode lse" + note)
+    return out, lse
+
+
+@pytest.mark.parametrize("D,G", [(128, 4), (128, 8), (64, 2), (64, 1)])
+def test_fused_append_decode_small(D, G):
+    """The new token's slot holds NaN before the call: reading it instead of
+    the substituted row would show in every output of that sequence."""
+    Hkv = 2
+    cfg = workloads.DecodeConfig("f", 9, G * Hkv, Hkv, D, 16, 0, 1500, 4)
+    d = workloads.make_decode_inputs(cfg, seed=17, ctx=[0, 15, 16, 511, 512, 1023, 1024, 1300, 1500])
+    _fused_and_check(d, f" D={D} G={G}")
+
+
+def test_fused_append_decode_full_workload():
+    d = workloads.make_decode_inputs(workloads.DECODE_CONFIGS["decode"], seed=0)
+    out, lse = _fused_and_check(d, " full")
+    # and the same numbers as the two-launch path on the same inputs
+    g = _dev(d)
+    lib.kv_append(g["k_cache"], g["v_cache"], g["block_table"], g["pos"], g["k_new"], g["v_new"])
+    o2, l2 = lib.paged_decode_attn(g["q"], g["k_cache"], g["v_cache"], g["block_table"], g["ctx_lens"], d.scale,
+                                   return_lse=True)
+    assert torch.equal(out, o2) and torch.equal(lse, l2)
+
+
+def test_fused_append_idle_and_out_of_table_positions():
+    d = workloads.make_decode_inputs(SMALL, seed=18, ctx=[5, 6, 7, 8, 9, 10, 11])
+    g = _dev(d)
+    pos = g["pos"].clone()
+    pos[1] = -1  # idle: cache untouched, empty result
+    pos[2] = 16 * d.block_table.shape[1]  # past the table: reported, cache untouched
+    before = g["k_cache"].cpu().view(torch.int16).numpy().copy()
+    ws = lib.Workspace(lib.paged_decode_workspace_size(7, 8, d.block_table.shape[1], 16, 128))
+    out, lse = lib.paged_decode_attn_append(g["q"], g["k_new"], g["v_new"], g["k_cache"], g["v_cache"],
+                                            g["block_table"], pos, d.scale, return_lse=True, workspace=ws)
+    assert ws.status() == 5
+    assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
+    got = g["k_cache"].cpu().view(torch.int16).numpy()
+    for b in (1, 2):
+        p = int(d.pos[b])
+        blk, slot = int(d.block_table[b, p // 16]), p % 16
+        assert np.array_equal(got[blk, :, slot], before[blk, :, slot])
+    keep = [0, 3, 4, 5, 6]
+    ek, ev = oracle.kv_append(d.k_cache, d.v_cache, d.block_table[keep], d.pos[keep], d.k_new[keep], d.v_new[keep])
+    ro, rl = oracle.paged_decode(d.q[keep], torch.from_numpy(ek).view(torch.bfloat16),
+                                 torch.from_numpy(ev).view(torch.bfloat16), d.block_table[keep], d.ctx_lens[keep],
+                                 d.scale)
+    assert_out_close(out[keep], ro)
+    assert_lse_close(lse[keep], rl)
