@@ -255,6 +255,43 @@ attn_status paged_decode_attn_append(const attn_tensor *q, const attn_tensor *k_
                                      void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * paged_prefill_attn -- a chunk of T new tokens per sequence: write their K/V
+ * into the paged cache and attend with their queries over the cache ("KV
+ * cache in nanoVLM", prefill phase: the prompt is encoded in one pass and its
+ * K/V fill the cache; "LLM inference memory accounting", section 20: a long
+ * prompt may be prefilled chunk by chunk, which changes the schedule, not the
+ * result).
+ *
+ * Sequence b holds start_pos[b] tokens before the chunk; chunk token i sits at
+ * position p = start_pos[b] + i.  With k_new / v_new given, first
+ *     cache.k[block_table[b][p/16], g, p % 16, :] = k_new[b, g, i, :]  (v likewise)
+ * (both NULL: the chunk is already in the cache).  Then for every query head
+ * h, with g = h / (Hq / Hkv), query i attends over the tokens t < n of KV
+ * head g, read through the block table as in paged_decode_attn:
+ *     n = p + 1                 causal = 1 (no token after its own position)
+ *     n = start_pos[b] + T      causal = 0 (the whole chunk)
+ *     out[b,h,i,:] = sum_t softmax(s)_t V[t],  lse[b,h,i] = log sum_t exp(s_t),
+ *     s_t = scale * <q[b,h,i,:], K[t]>.
+ * start_pos[b] < 0 or start_pos[b] + T > max_blocks * 16 sets
+ * ATTN_ERR_DEVICE_BOUNDS, leaves that sequence's cache alone and writes its
+ * outputs as out = 0, lse = -inf; a bad block id sets the same flag.
+ *
+ *   q, out       [batch, Hq, T, head_dim]; q bf16, out bf16 or f32 (strided views,
+ *                16-byte aligned rows)
+ *   k_new, v_new [batch, Hkv, T, head_dim] bf16, or both NULL
+ *   start_pos    int32 [batch]
+ *   lse          float32 [batch, Hq, T] contiguous, or NULL
+ *   workspace    >= attn_fwd_workspace_size() bytes (the status word)
+ * Cache head_dim 64 or 128.  Blocks of the chunk must not be shared with
+ * another sequence of the same call.
+ */
+attn_status paged_prefill_attn(const attn_tensor *q, const attn_tensor *k_new, const attn_tensor *v_new,
+                               const attn_kv_cache *cache, const int32_t *block_table, int64_t bt_stride,
+                               int32_t max_blocks, const int32_t *start_pos, int32_t causal, float scale,
+                               const attn_tensor *out, float *lse,
+                               void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * paged_decode_attn_noalloc -- the same paged decode for callers that cannot
  * allocate device memory.  The pages have no counterpart to this call; it
  * exists for this library's users.

@@ -86,6 +86,7 @@ def load(build_if_missing: bool = False):
             "kv_append": (I32, [C, P, I64, I32, P, T, T, P, SZ, P]),
             "paged_decode_attn": (I32, [T, C, P, I64, I32, P, F, T, P, P, SZ, P]),
             "paged_decode_attn_append": (I32, [T, T, T, C, P, I64, I32, P, F, T, P, P, SZ, P]),
+            "paged_prefill_attn": (I32, [T, T, T, C, P, I64, I32, P, I32, F, T, P, P, SZ, P]),
             "paged_kv_gather": (I32, [C, I32, P, I64, I32, P, I32, I64, P, P, SZ, P]),
             "paged_decode_attn_noalloc": (I32, [T, C, P, I64, I32, P, F, T, P, P, P]),
             "attn_check_device_status": (I32, [P, ctypes.POINTER(ctypes.c_uint32), P]),
@@ -105,7 +106,7 @@ def exported_symbols() -> list[str]:
             "attn_fwd_workspace_size", "kv_append_workspace_size", "paged_decode_workspace_size",
             "attn_check_device_status", "attn_reset_device_status", "attn_status_string", "attn_version",
             "paged_decode_attn_noalloc", "attn_selftest_wait_timeout", "attn_fwd_varlen",
-            "attn_key_padding_to_additive", "paged_decode_attn_append"]
+            "attn_key_padding_to_additive", "paged_decode_attn_append", "paged_prefill_attn"]
 
 
 # --------------------------------------------------------------------------
@@ -374,6 +375,37 @@ def paged_decode_attn_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.
                                       float(scale), ctypes.byref(do), _ptr(lse), ws.ptr, ws.nbytes,
                                       _stream(stream))
     _check("paged_decode_attn_append", st)
+    return (out, lse) if return_lse else out
+
+
+def paged_prefill_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.Tensor,
+                       start_pos: torch.Tensor, k_new: Optional[torch.Tensor] = None,
+                       v_new: Optional[torch.Tensor] = None, causal: bool = True, scale: Optional[float] = None,
+                       out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                       return_lse: bool = False, workspace: Optional[Workspace] = None, stream=None):
+    """A chunk of T tokens per sequence: q [B, Hq, T, D] at positions
+    start_pos[b] + i.  With k_new / v_new ([B, Hkv, T, D]) their K/V are
+    first written to the cache; queries then attend over the cache through
+    the block table (causal: up to their own position)."""
+    lib = load()
+    B, Hq, T, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1
+    assert start_pos.dtype == torch.int32 and start_pos.is_contiguous()
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    ws = workspace or _small_ws(q.device)
+    c = _cache(k_cache, v_cache)
+    dq, do = _desc(q), _desc(out)
+    dk = ctypes.byref(_desc(k_new)) if k_new is not None else None
+    dv = ctypes.byref(_desc(v_new)) if v_new is not None else None
+    st = lib.paged_prefill_attn(ctypes.byref(dq), dk, dv, ctypes.byref(c), block_table.data_ptr(),
+                                block_table.stride(0), block_table.shape[1], start_pos.data_ptr(), int(bool(causal)),
+                                float(scale), ctypes.byref(do), _ptr(lse), ws.ptr, ws.nbytes, _stream(stream))
+    _check("paged_prefill_attn", st)
     return (out, lse) if return_lse else out
 
 

@@ -360,6 +360,62 @@ attn_status paged_decode_attn_append(const attn_tensor* q, const attn_tensor* k_
                            workspace, workspace_bytes, stream);
 }
 
+attn_status paged_prefill_attn(const attn_tensor* q, const attn_tensor* k_new, const attn_tensor* v_new,
+                               const attn_kv_cache* cache, const int32_t* block_table, int64_t bt_stride,
+                               int32_t max_blocks, const int32_t* start_pos, int32_t causal, float scale,
+                               const attn_tensor* out, float* lse, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+  attn_status st;
+  if ((st = check_cache(cache)) != ATTN_OK) return st;
+  if ((st = check_tensor(q, 4)) != ATTN_OK) return st;
+  if ((st = check_tensor(out, 4)) != ATTN_OK) return st;
+  const int64_t B = q->shape[0], Hq = q->shape[1], T = q->shape[2], D = q->shape[3];
+  for (int i = 0; i < 4; ++i)
+    if (out->shape[i] != q->shape[i]) return ATTN_ERR_INVALID_ARG;
+  if (q->dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (D != cache->head_dim) return ATTN_ERR_INVALID_ARG;
+  if (Hq <= 0 || Hq % cache->num_kv_heads != 0) return ATTN_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (max_blocks <= 0 || max_blocks > (1 << 24)) return ATTN_ERR_INVALID_ARG;
+  if (B > 65535 || Hq > 65535 || T > (int64_t(1) << 30) || cache->num_blocks > 0x7fffffff)
+    return ATTN_ERR_UNSUPPORTED;
+  if ((k_new == nullptr) != (v_new == nullptr)) return ATTN_ERR_INVALID_ARG;
+  if (k_new != nullptr) {
+    if ((st = check_tensor(k_new, 4)) != ATTN_OK) return st;
+    if ((st = check_tensor(v_new, 4)) != ATTN_OK) return st;
+    if (k_new->dtype != ATTN_BF16 || v_new->dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
+    const int64_t want[4] = {B, cache->num_kv_heads, T, D};
+    for (int i = 0; i < 4; ++i)
+      if (k_new->shape[i] != want[i] || v_new->shape[i] != want[i]) return ATTN_ERR_INVALID_ARG;
+  }
+  if ((st = check_workspace(workspace, workspace_bytes, kStatusBytes)) != ATTN_OK) return st;
+  if (B == 0 || T == 0) return ATTN_OK;
+  if (block_table == nullptr || start_pos == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (B > 1 && bt_stride < max_blocks) return ATTN_ERR_INVALID_ARG;
+  if (!vec16_ok(q) || !vec16_ok(out)) return ATTN_ERR_INVALID_ARG;
+  if (k_new != nullptr && (!vec16_ok(k_new) || !vec16_ok(v_new))) return ATTN_ERR_INVALID_ARG;
+  PrefillArgs a;
+  a.cache = paged(cache);
+  a.q = view(q);
+  a.out = view(out);
+  a.k_new = k_new != nullptr ? view(k_new) : View4{};
+  a.v_new = v_new != nullptr ? view(v_new) : View4{};
+  a.block_table = block_table;
+  a.bt_stride = bt_stride;
+  a.max_blocks = max_blocks;
+  a.start_pos = start_pos;
+  a.causal = causal;
+  a.B = B;
+  a.Hq = Hq;
+  a.T = T;
+  a.scale = scale;
+  a.lse = lse;
+  a.status = static_cast<uint32_t*>(workspace);
+  if (k_new != nullptr && (st = from_cuda(launch_kv_append_chunk(a, stream))) != ATTN_OK) return st;
+  return from_cuda(launch_paged_prefill_tc(a, stream));
+}
+
 attn_status attn_selftest_wait_timeout(void* workspace, size_t workspace_bytes, uint32_t timeout_us,
                                        cudaStream_t stream) {
   attn_status st;

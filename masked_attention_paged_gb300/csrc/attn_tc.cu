@@ -33,6 +33,19 @@
 //               finally normalises O and writes out / lse.
 // TMEM columns: S_A [0,128), S_B [128,256), O_A [256,256+D), O_B after it.
 //
+// Paged instances (PAGED) serve chunked prefill over a paged KV cache ("KV
+// cache in nanoVLM", prefill phase; "LLM inference memory accounting",
+// sections 15 and 20): the queries are a chunk of T new tokens at positions
+// start + i of their sequence, and each 128-key tile is gathered from eight
+// 16-token cache blocks through the block table, one 16-row TMA box per
+// block at its row offset (the 128-byte swizzle repeats every 8 rows, so the
+// tile's shared-memory image is the same as a 128-row load).  Keys past a
+// row's limit (its own position when causal, the sequence end otherwise) are
+// selected to -inf rather than masked by addition, so whatever an unfilled
+// cache slot holds never reaches the softmax; V rows past the CTA's last key
+// are zeroed in shared memory before the last PV, as P = 0 times a NaN would
+// not be 0.
+//
 // Every wait is bounded (common.cuh): a hang turns into ATTN_ERR_TIMEOUT in
 // the caller's status word and the CTA winds down and frees its TMEM.
 #include <cuda.h>
@@ -109,6 +122,13 @@ struct TcParams {
   const float* mask;
   int64_t mask_stride;
   const int32_t* key_lens;  // per-batch valid keys, or null (all Pk)
+  // PAGED: cache read through the block table
+  const int32_t* bt;
+  int64_t bt_stride;
+  int max_blocks;
+  int num_blocks;
+  const int32_t* start_pos;  // [B] tokens cached before the chunk
+  int causal;
   void* out;
   int64_t out_stride[3];  // b, h, row (elements)
   float* lse;
@@ -122,7 +142,7 @@ __device__ __forceinline__ void coords(const TmaCoordMap& m, int p, int h, int b
   c3 = m.slot_p == 3 ? p : (m.slot_h == 3 ? h : b);
 }
 
-template <int D, bool OUT_BF16>
+template <int D, bool OUT_BF16, bool PAGED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
@@ -136,10 +156,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int h = blockIdx.y;
   const int b = blockIdx.z;
   const int g = h / prm.group;
-  const int q0 = blockIdx.x * (2 * kBM);
   // keys of this batch row: all Pk, or its valid length (tiles past it are skipped)
+  int q0 = blockIdx.x * (2 * kBM);
   int n_keys = prm.Pk;
-  if (prm.key_lens != nullptr) {
+  int start = 0;  // PAGED: position of the chunk's first token
+  if constexpr (PAGED) {
+    // causal: the longest query tiles (latest positions) first
+    if (prm.causal) q0 = (gridDim.x - 1 - blockIdx.x) * (2 * kBM);
+    start = prm.start_pos[b];
+    const int64_t seq_len = static_cast<int64_t>(start) + prm.Pq;
+    if (start < 0 || seq_len > static_cast<int64_t>(prm.max_blocks) * 16) {
+      if (threadIdx.x == 0 && blockIdx.x == 0 && h == 0) report(prm.status, kStatusBounds);
+      n_keys = 0;  // the sequence is written as zeros
+    } else {
+      // the last key any row of this CTA may see
+      n_keys = prm.causal ? start + min(q0 + 2 * kBM, prm.Pq) : static_cast<int>(seq_len);
+    }
+  } else if (prm.key_lens != nullptr) {
     const int len = prm.key_lens[b];
     n_keys = len < 0 ? 0 : (len < prm.Pk ? len : prm.Pk);
   }
@@ -201,22 +234,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nkv; ++j) {
         const int s = j % C::kStages;
         const uint32_t ph = (j / C::kStages) & 1;
-        if (!mbar_wait(&bars->k_empty[s], ph ^ 1, abort, prm.status)) break;
-        mbar_arrive_expect_tx(&bars->k_full[s], C::kTileBytes);
-        coords(prm.ck, j * kBN, g, b, c1, c2, c3);
+        if constexpr (PAGED) {
+          // the tile's keys sit in logical blocks 8j .. 8j+7; blocks wholly
+          // past the CTA's last key are not loaded, nor is a bad block id
+          constexpr int kBlk = kBN / 16;
+          const int nb = min(kBlk, (n_keys - j * kBN + 15) / 16);
+          const int32_t* row = prm.bt + static_cast<int64_t>(b) * prm.bt_stride + j * kBlk;
+          int ids[kBlk];
+          int n_ok = 0;
 #pragma unroll
-        for (int x = 0; x < C::kBoxes; ++x)
-          tma_load_4d(smem + C::kOffK + s * C::kTileBytes + x * kBoxBytes, &tm_k, &bars->k_full[s], x * 64,
-                      c1, c2, c3);
-        k_issued = j + 1;
-        if (!mbar_wait(&bars->v_empty[s], ph ^ 1, abort, prm.status)) break;
-        mbar_arrive_expect_tx(&bars->v_full[s], C::kTileBytes);
-        coords(prm.cv, j * kBN, g, b, c1, c2, c3);
+          for (int i = 0; i < kBlk; ++i) {
+            ids[i] = -1;
+            if (i < nb) {
+              const int id = row[i];
+              if (id < 0 || id >= prm.num_blocks) {
+                report(prm.status, kStatusBounds);
+              } else {
+                ids[i] = id;
+                ++n_ok;
+              }
+            }
+          }
+          constexpr int kBlockBytes = 16 * D * 2;
+          if (!mbar_wait(&bars->k_empty[s], ph ^ 1, abort, prm.status)) break;
+          mbar_arrive_expect_tx(&bars->k_full[s], n_ok * kBlockBytes);
 #pragma unroll
-        for (int x = 0; x < C::kBoxes; ++x)
-          tma_load_4d(smem + C::kOffV + s * C::kTileBytes + x * kBoxBytes, &tm_v, &bars->v_full[s], x * 64,
-                      c1, c2, c3);
-        v_issued = j + 1;
+          for (int i = 0; i < kBlk; ++i)
+            if (ids[i] >= 0)
+#pragma unroll
+              for (int x = 0; x < C::kBoxes; ++x)
+                tma_load_4d(smem + C::kOffK + s * C::kTileBytes + x * kBoxBytes + i * 2048, &tm_k, &bars->k_full[s],
+                            x * 64, 0, g, ids[i]);
+          k_issued = j + 1;
+          if (!mbar_wait(&bars->v_empty[s], ph ^ 1, abort, prm.status)) break;
+          mbar_arrive_expect_tx(&bars->v_full[s], n_ok * kBlockBytes);
+#pragma unroll
+          for (int i = 0; i < kBlk; ++i)
+            if (ids[i] >= 0)
+#pragma unroll
+              for (int x = 0; x < C::kBoxes; ++x)
+                tma_load_4d(smem + C::kOffV + s * C::kTileBytes + x * kBoxBytes + i * 2048, &tm_v, &bars->v_full[s],
+                            x * 64, 0, g, ids[i]);
+          v_issued = j + 1;
+        } else {
+          if (!mbar_wait(&bars->k_empty[s], ph ^ 1, abort, prm.status)) break;
+          mbar_arrive_expect_tx(&bars->k_full[s], C::kTileBytes);
+          coords(prm.ck, j * kBN, g, b, c1, c2, c3);
+#pragma unroll
+          for (int x = 0; x < C::kBoxes; ++x)
+            tma_load_4d(smem + C::kOffK + s * C::kTileBytes + x * kBoxBytes, &tm_k, &bars->k_full[s], x * 64,
+                        c1, c2, c3);
+          k_issued = j + 1;
+          if (!mbar_wait(&bars->v_empty[s], ph ^ 1, abort, prm.status)) break;
+          mbar_arrive_expect_tx(&bars->v_full[s], C::kTileBytes);
+          coords(prm.cv, j * kBN, g, b, c1, c2, c3);
+#pragma unroll
+          for (int x = 0; x < C::kBoxes; ++x)
+            tma_load_4d(smem + C::kOffV + s * C::kTileBytes + x * kBoxBytes, &tm_v, &bars->v_full[s], x * 64,
+                        c1, c2, c3);
+          v_issued = j + 1;
+        }
       }
       if (*abort) {
         // let every copy still in flight land before the CTA exits
@@ -354,7 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float kLog2e = 1.4426950408889634f;
     const float* mrow = prm.mask ? prm.mask + static_cast<int64_t>(b) * prm.mask_stride : nullptr;
     float* mbuf = reinterpret_cast<float*>(smem + C::kOffMask);
-    for (int j = 0; j < nkv; ++j) {
+    // paged instances have no mask tensor: the softmax applies the row limits
+    for (int j = 0; j < (PAGED ? 0 : nkv); ++j) {
       const int s = j & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->m_empty[s], ((j >> 1) & 1) ^ 1, abort, prm.status))) break;
       float v[4];
@@ -387,12 +465,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = -INFINITY;  // reference max, log2 units
     float l_run = 0.0f;       // running sum of 2^(x - m_run)
     bool ok = true;
+    // PAGED: keys [0, row_lim) are this row's (its own position when causal)
+    int row_lim = n_keys;
+    if constexpr (PAGED) {
+      if (prm.causal) row_lim = min(n_keys, start + q0 + t * kBM + row + 1);
+    }
 
     for (int j = 0; j < nkv; ++j) {
       const int mb_i = j & 1;
       // wait outcomes are made warp-uniform: tcgen05.ld/st need the whole warp
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], j & 1, abort, prm.status) &&
-                                       mbar_wait(&bars->m_full[mb_i], (j >> 1) & 1, abort, prm.status))) {
+                                       (PAGED || mbar_wait(&bars->m_full[mb_i], (j >> 1) & 1, abort, prm.status)))) {
         ok = false;
         break;
       }
@@ -400,7 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t sr[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_addr + s_col + c * 32, sr[c]);
-      const bool masked_tile = bars->m_flag[mb_i] != 0;
+      // keys of this tile the row may see: [0, lim)
+      const int lim = row_lim - j * kBN;
+      const bool masked_tile = PAGED ? __any_sync(0xffffffffu, lim < kBN) || !prm.scale_positive
+                                     : bars->m_flag[mb_i] != 0;
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
       if constexpr (C::kSepP) {  // S is in registers: the next S may overwrite it
@@ -450,6 +536,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 8; ++i) mx[i] = fmaxf(SV(2 * i), SV(2 * i + 1));
 #pragma unroll
           for (int c = 16; c < kBN; c += 2) mx[(c >> 1) & 7] = fmax3(mx[(c >> 1) & 7], SV(c), SV(c + 1));
+        } else if constexpr (PAGED) {
+          // logits, keys past the row's limit selected to -inf, in place
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) {
+            const float x = c < lim ? SV(c) * prm.scale_log2 : -INFINITY;
+            sr[c >> 5][c & 31] = __float_as_uint(x);
+            mx[(c >> 1) & 7] = fmaxf(mx[(c >> 1) & 7], x);
+          }
         } else {
           // logits with the additive mask, in place
           const float4* mb = reinterpret_cast<const float4*>(mbuf + mb_i * kBN);
@@ -536,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #undef SV
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->m_empty[mb_i]);  // this warp is done with the mask tile
+      if (!PAGED && lane == 0) mbar_arrive(&bars->m_empty[mb_i]);  // this warp is done with the mask tile
       l_run = l_run * alpha + rs;
 
       // O_t is stable here: PV_t(j-1) has completed (o_done, or the commit
@@ -550,6 +646,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
           tmem_st32(tmem + lane_addr + o_col + c * 32, o);
+        }
+      }
+      if constexpr (PAGED) {
+        // last tile: V rows past the CTA's last key were not loaded (or hold
+        // whatever the cache's unfilled slots hold); zero them before PV reads
+        // them.  Both softmax warpgroups write the same zeros.  The stage is
+        // not refilled before this warpgroup's p_full below.
+        const int r0 = n_keys - j * kBN;
+        if (j == nkv - 1 && r0 < kBN) {
+          const int s = j % C::kStages;
+          if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[s], (j / C::kStages) & 1, abort, prm.status))) {
+            ok = false;
+            break;
+          }
+          uint8_t* vst = smem + C::kOffV + s * C::kTileBytes;
+          const int nchunk = (kBN - r0) * 8;  // 16-byte chunks of the rows past r0, per box
+#pragma unroll
+          for (int x = 0; x < C::kBoxes; ++x)
+            for (int c = row; c < nchunk; c += kBM)
+              *reinterpret_cast<uint4*>(vst + x * kBoxBytes + (r0 + c / 8) * 128 + (c % 8) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();  // the generic-proxy stores before the MMA's async-proxy reads
         }
       }
       tmem_wait_st();
@@ -679,10 +797,28 @@ bool make_map(CUtensorMap* map, TmaCoordMap* cm, const View4& t) {
   return r == CUDA_SUCCESS;
 }
 
+// A 4-D bf16 tensor map over one paged cache tensor [num_blocks, Hkv, 16, D]
+// (contiguous): dims (D, slot, head, block), box 64 columns x 16 slots of one
+// head of one block, 128-byte swizzle.
+bool make_cache_map(CUtensorMap* map, void* base, int64_t num_blocks, int Hkv, int D) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), 16, static_cast<cuuint64_t>(Hkv),
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(16) * D * 2,
+                                 static_cast<cuuint64_t>(Hkv) * 16 * D * 2};
+  const cuuint32_t box[4] = {64, 16, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int D, bool OUT_BF16>
 cudaError_t launch_tc(const AttnFwdArgs& a, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
-  TcParams p;
+  TcParams p = {};
   if (!make_map(&mq, &p.cq, a.q) || !make_map(&mk, &p.ck, a.k) || !make_map(&mv, &p.cv, a.v))
     return cudaErrorInvalidValue;
   p.Pq = static_cast<int>(a.Pq);
@@ -700,11 +836,46 @@ cudaError_t launch_tc(const AttnFwdArgs& a, cudaStream_t stream) {
   p.out_stride[2] = a.out.stride[2];
   p.lse = a.lse;
   p.status = a.status;
-  auto kern = attn_fwd_tc_kernel<D, OUT_BF16>;
+  auto kern = attn_fwd_tc_kernel<D, OUT_BF16, false>;
   const int smem = Cfg<D>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>((a.Pq + 2 * kBM - 1) / (2 * kBM)), static_cast<unsigned>(a.Hq),
+            static_cast<unsigned>(a.B));
+  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+template <int D, bool OUT_BF16>
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  TcParams p = {};
+  if (!make_map(&mq, &p.cq, a.q) || !make_cache_map(&mk, a.cache.k, a.cache.num_blocks, a.cache.Hkv, D) ||
+      !make_cache_map(&mv, a.cache.v, a.cache.num_blocks, a.cache.Hkv, D))
+    return cudaErrorInvalidValue;
+  p.Pq = static_cast<int>(a.T);
+  p.Pk = 0;
+  p.Hq = static_cast<int>(a.Hq);
+  p.group = static_cast<int>(a.Hq / a.cache.Hkv);
+  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  p.scale_positive = p.scale_log2 > 0.0f;
+  p.bt = a.block_table;
+  p.bt_stride = a.bt_stride;
+  p.max_blocks = a.max_blocks;
+  p.num_blocks = static_cast<int>(a.cache.num_blocks);
+  p.start_pos = a.start_pos;
+  p.causal = a.causal;
+  p.out = a.out.data;
+  p.out_stride[0] = a.out.stride[0];
+  p.out_stride[1] = a.out.stride[1];
+  p.out_stride[2] = a.out.stride[2];
+  p.lse = a.lse;
+  p.status = a.status;
+  auto kern = attn_fwd_tc_kernel<D, OUT_BF16, true>;
+  const int smem = Cfg<D>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(static_cast<unsigned>((a.T + 2 * kBM - 1) / (2 * kBM)), static_cast<unsigned>(a.Hq),
             static_cast<unsigned>(a.B));
   kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
@@ -716,6 +887,14 @@ cudaError_t launch_attn_fwd_tc(const AttnFwdArgs& a, cudaStream_t stream) {
   const bool bf16_out = a.out.dtype == ATTN_BF16;
   if (a.D == 64) return bf16_out ? launch_tc<64, true>(a, stream) : launch_tc<64, false>(a, stream);
   if (a.D == 128) return bf16_out ? launch_tc<128, true>(a, stream) : launch_tc<128, false>(a, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_paged_prefill_tc(const PrefillArgs& a, cudaStream_t stream) {
+  const bool bf16_out = a.out.dtype == ATTN_BF16;
+  if (a.cache.D == 64) return bf16_out ? launch_prefill<64, true>(a, stream) : launch_prefill<64, false>(a, stream);
+  if (a.cache.D == 128)
+    return bf16_out ? launch_prefill<128, true>(a, stream) : launch_prefill<128, false>(a, stream);
   return cudaErrorInvalidValue;
 }
 

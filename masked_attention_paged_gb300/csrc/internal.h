@@ -101,6 +101,25 @@ int decode_num_splits(int max_blocks, int block_size);
 size_t decode_partial_bytes(int64_t B, int64_t Hq, int n_split, int D);
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);
 
+struct PrefillArgs {
+  PagedCache cache;
+  View4 q, out;        // [B, Hq, T, D]
+  View4 k_new, v_new;  // [B, Hkv, T, D]; data null when the chunk is already cached
+  const int32_t* block_table;
+  int64_t bt_stride;
+  int max_blocks;
+  const int32_t* start_pos;  // [B] tokens cached before the chunk
+  int causal;
+  int64_t B, Hq, T;
+  float scale;
+  float* lse;  // [B, Hq, T] or null
+  uint32_t* status;
+};
+// write the chunk's K/V to positions start_pos[b] + i of each sequence
+cudaError_t launch_kv_append_chunk(const PrefillArgs& a, cudaStream_t stream);
+// the chunk's queries over the paged cache (tcgen05 kernel, paged instance)
+cudaError_t launch_paged_prefill_tc(const PrefillArgs& a, cudaStream_t stream);
+
 // boolean key-padding mask (non-zero = padded) -> additive 0 / -inf
 cudaError_t launch_padding_mask_to_additive(const uint8_t* kpm, int64_t kpm_stride, int64_t B, int64_t Pk,
                                             float* out, int64_t out_stride, cudaStream_t stream);

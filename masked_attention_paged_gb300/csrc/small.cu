@@ -62,6 +62,58 @@ __global__ void kv_append_kernel(const AppendParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// kv_append_chunk: token i of sequence b's chunk (k_new[b, g, i, :]) goes to
+// position start_pos[b] + i.  grid (vector tiles, B); 16-byte vectors, the
+// dim chunk fastest, then the token, then the head, so consecutive threads
+// read one head's rows of the chunk and write whole cache blocks.
+// ---------------------------------------------------------------------------
+struct ChunkAppendParams {
+  uint16_t* kc;
+  uint16_t* vc;
+  int64_t num_blocks;
+  int Hkv, D, T;
+  const int32_t* bt;
+  int64_t bt_stride;
+  int max_blocks;
+  const int32_t* start_pos;
+  const uint16_t* kn;
+  const uint16_t* vn;
+  int64_t kn_stride[3], vn_stride[3];  // batch, head, token (elements)
+  uint32_t* status;
+};
+
+__global__ void kv_append_chunk_kernel(const ChunkAppendParams p) {
+  constexpr int kBS = 16;
+  const int b = blockIdx.y;
+  const int start = p.start_pos[b];
+  if (start < 0 || static_cast<int64_t>(start) + p.T > static_cast<int64_t>(p.max_blocks) * kBS) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) report(p.status, kStatusBounds);
+    return;  // the whole sequence is skipped, as its attention is
+  }
+  const int vpr = p.D / 8;
+  const int64_t n = static_cast<int64_t>(p.Hkv) * p.T * vpr;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(idx % vpr);
+    const int i = static_cast<int>((idx / vpr) % p.T);
+    const int g = static_cast<int>(idx / (static_cast<int64_t>(vpr) * p.T));
+    const int t = start + i;
+    const int blk = p.bt[static_cast<int64_t>(b) * p.bt_stride + t / kBS];
+    if (blk < 0 || blk >= p.num_blocks) {
+      report(p.status, kStatusBounds);
+      continue;
+    }
+    const int64_t dst = ((static_cast<int64_t>(blk) * p.Hkv + g) * kBS + t % kBS) * p.D + c * 8;
+    const uint4 kv = *reinterpret_cast<const uint4*>(p.kn + b * p.kn_stride[0] + g * p.kn_stride[1] +
+                                                     i * p.kn_stride[2] + c * 8);
+    const uint4 vv = *reinterpret_cast<const uint4*>(p.vn + b * p.vn_stride[0] + g * p.vn_stride[1] +
+                                                     i * p.vn_stride[2] + c * 8);
+    *reinterpret_cast<uint4*>(p.kc + dst) = kv;
+    *reinterpret_cast<uint4*>(p.vc + dst) = vv;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // paged_gather: dst[b, g, t, :] = cache[block_table[b][t / bs], g, t % bs, :]
 // grid (token tiles of 16, Hkv, B); 16-byte vectors.
 // ---------------------------------------------------------------------------
@@ -237,6 +289,32 @@ cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
   p.status = a.status;
   const int threads = std::min(256, std::max(32, a.cache.Hkv * a.cache.D / 8));
   kv_append_kernel<<<static_cast<unsigned>(a.B), threads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_append_chunk(const PrefillArgs& a, cudaStream_t stream) {
+  ChunkAppendParams p;
+  p.kc = static_cast<uint16_t*>(a.cache.k);
+  p.vc = static_cast<uint16_t*>(a.cache.v);
+  p.num_blocks = a.cache.num_blocks;
+  p.Hkv = a.cache.Hkv;
+  p.D = a.cache.D;
+  p.T = static_cast<int>(a.T);
+  p.bt = a.block_table;
+  p.bt_stride = a.bt_stride;
+  p.max_blocks = a.max_blocks;
+  p.start_pos = a.start_pos;
+  p.kn = static_cast<const uint16_t*>(a.k_new.data);
+  p.vn = static_cast<const uint16_t*>(a.v_new.data);
+  for (int i = 0; i < 3; ++i) {
+    p.kn_stride[i] = a.k_new.stride[i];
+    p.vn_stride[i] = a.v_new.stride[i];
+  }
+  p.status = a.status;
+  const int64_t n = static_cast<int64_t>(p.Hkv) * p.T * (p.D / 8);
+  const int64_t blocks = (n + 255) / 256;
+  dim3 grid(static_cast<unsigned>(blocks < 4096 ? blocks : 4096), static_cast<unsigned>(a.B));
+  kv_append_chunk_kernel<<<grid, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -248,3 +248,26 @@ def test_fused_decode_rejects(L):
     assert call(v=_t([4, 8, 128], 0)) == INVALID  # f32
     assert call(k=_t([3, 8, 128]), v=_t([3, 8, 128])) == INVALID  # batch differs from q
     assert call(ws_bytes=need - 256) == WORKSPACE
+
+
+def test_paged_prefill_rejects(L):
+    def call(q=None, k=None, v=None, c=None, sp=FAKE, causal=1, out=None, ws=FAKE, scale=0.1, bts=10):
+        q = q or _t([2, 8, 40, 128])
+        out = out or _t([2, 8, 40, 128])
+        c = c or _cache()
+        return L.paged_prefill_attn(ctypes.byref(q), None if k is None else ctypes.byref(k),
+                                    None if v is None else ctypes.byref(v), ctypes.byref(c), FAKE, bts, 10, sp,
+                                    causal, scale, ctypes.byref(out), None, ws, 256, None)
+    kn = _t([2, 8, 40, 128])
+    assert call(k=kn) == INVALID  # k_new without v_new
+    assert call(k=_t([2, 8, 39, 128]), v=_t([2, 8, 39, 128])) == INVALID  # chunk length differs from q
+    assert call(k=_t([2, 4, 40, 128]), v=_t([2, 4, 40, 128])) == INVALID  # heads differ from the cache
+    assert call(q=_t([2, 8, 40, 128], 0), out=_t([2, 8, 40, 128], 0)) == UNSUPPORTED  # f32 queries
+    assert call(q=_t([2, 8, 40, 64]), out=_t([2, 8, 40, 64])) == INVALID  # D differs from the cache
+    assert call(q=_t([2, 12, 40, 128]), out=_t([2, 12, 40, 128])) == INVALID  # 12 % 8
+    assert call(causal=2) == INVALID
+    assert call(sp=None) == INVALID
+    assert call(ws=None) == WORKSPACE
+    assert call(scale=float("nan")) == INVALID
+    assert call(bts=5) == INVALID
+    assert call(q=_t([2, 8, 0, 128]), out=_t([2, 8, 0, 128])) == OK  # empty chunk: nothing launched
