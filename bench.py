@@ -329,6 +329,65 @@ def e2e_steps(step, K, W):
     return ms, h2d, d2h
 
 
+def next_rows(step, K, W, pk):
+    """The widened calls, timed on their own after the step (not part of the
+    step's value): the fused append + decode on the decode workload, the
+    key-length form of the 32000-patch attention, and a causal chunked
+    prefill over a paged cache."""
+    lib = step.lib
+    dev = step.dev
+    d = step.dec
+    pf = workloads.make_prefill_inputs(workloads.PREFILL_CONFIGS["prefill_chunk"], seed=0)
+    p_q, p_kn, p_vn = pf.q.to(dev), pf.k_new.to(dev), pf.v_new.to(dev)
+    p_kc, p_vc, p_bt, p_sp = pf.k_cache.to(dev), pf.v_cache.to(dev), pf.block_table.to(dev), pf.start_pos.to(dev)
+    p_o = torch.empty_like(p_q)
+    p_l = torch.empty(p_q.shape[:3], dtype=torch.float32, device=dev)
+    pc = pf.cfg
+    p_flops = workloads.prefill_flops(pf.start_pos, pc.T, pc.Hq, pc.D, pc.causal)
+    lc = step.large.cfg
+    l_lens = torch.full((lc.B,), lc.Pk - step.large.n_pad, dtype=torch.int32, device=dev)
+
+    def fused():
+        lib.paged_decode_attn_append(step.dq, step.kn, step.vn, step.kc, step.vc, step.bt, step.pos, d.scale,
+                                     out=step.d_o, workspace=step.ws_dec)
+
+    def varlen():
+        lib.attn_fwd_varlen(step.l_q, step.l_k, step.l_v, l_lens, step.large.scale, out=step.l_o, lse=step.l_l,
+                            workspace=step.ws_attn)
+
+    def prefill():
+        lib.paged_prefill_attn(p_q, p_kc, p_vc, p_bt, p_sp, k_new=p_kn, v_new=p_vn, causal=True, scale=pf.scale,
+                               out=p_o, lse=p_l, workspace=step.ws_attn)
+
+    def time_it(fn):
+        for _ in range(W):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(K):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / K
+
+    f_ms, v_ms, p_ms = time_it(fused), time_it(varlen), time_it(prefill)
+    peak_t = pk["bf16_tflops_sustained"]
+    f_gbs = step.decode_bytes / (f_ms * 1e-3) / 1e9
+    v_tf = step.flops_large / (v_ms * 1e-3) / 1e12
+    p_tf = p_flops / (p_ms * 1e-3) / 1e12
+    return {
+        "paged_decode_attn_append": {"workload": "decode (64 seqs, Hq 32, Hkv 8, D 128, ctx U[512, 8192])",
+                                     "ms": f_ms, "gbs": f_gbs, "frac": f_gbs / pk["hbm_gbs"], "launches": 2},
+        "attn_fwd_varlen": {"workload": "patch_large with key lengths (B 1, H 16, P 32000, D 64, 128 padded keys)",
+                            "ms": v_ms, "tflops": v_tf, "frac": v_tf / peak_t, "launches": 1},
+        "paged_prefill_attn": {"workload": "prefill_chunk (16 seqs x 1024-token causal chunk after U[0, 7168] "
+                                           "cached, Hq 32, Hkv 8, D 128)",
+                               "ms": p_ms, "tflops": p_tf, "frac": p_tf / peak_t, "launches": 2,
+                               "flops": p_flops},
+    }
+
+
 # ---------------------------------------------------------------------------
 # the oracle on the host cores (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------
@@ -403,6 +462,7 @@ def main():
     ap.add_argument("--impl", default="libattn", choices=["libattn", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-next", action="store_true", help="skip timing the calls outside the step")
     args = ap.parse_args()
     rank, world, local = dist_init(args.gpus)
     if args.impl == "reference":
@@ -465,6 +525,8 @@ def main():
         "clocks": clk,
         "gpu_launches": step.launches_per_step * args.steps,
     }
+    if not args.no_next:
+        line["next"] = next_rows(step, max(5, args.steps // 2), max(3, args.warmup), pk)
     if not args.no_e2e:
         e_ms, h2d, d2h = e2e_steps(step, max(3, args.steps // 4), 2)
         e_ms = max_over_ranks(e_ms, world)
