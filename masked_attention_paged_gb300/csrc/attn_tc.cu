@@ -489,42 +489,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                                      : bars->m_flag[mb_i] != 0;
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
+#define SV(c) __uint_as_float(sr[(c) >> 5][(c) & 31])
       if constexpr (C::kSepP) {  // S is in registers: the next S may overwrite it
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars->s_free[t]);
       }
-#define SV(c) __uint_as_float(sr[(c) >> 5][(c) & 31])
 
       float alpha = 1.0f;
       float rs = 0.0f;
       bool done = false;
-      if constexpr (!C::kSepP) {
-        // Fast path: exponentiate against the current reference max without a
-        // max pass.  Every term is <= 2^64 exactly when the row sum is, which
-        // keeps the sums far from fp32 overflow; if some row fails, the warp
-        // reloads S (its columns are intact until P is written over them) and
-        // takes the full path below.
-        if (!masked_tile && __all_sync(0xffffffffu, m_run != -INFINITY)) {
-          float rsum[8];
+      // Fast path (P over S only): exponentiate against the current reference
+      // max without a max pass.  Every term is <= 2^64 exactly when the row
+      // sum is, which keeps the sums far from fp32 overflow; if some row
+      // fails, the warp reloads S (its columns are intact until P is written
+      // over them) and takes the full path below.  With P apart from S, S's
+      // columns are handed back right after the load, which is worth more
+      // than skipping the max pass.
+      const bool try_fast = !C::kSepP && !masked_tile && __all_sync(0xffffffffu, m_run != -INFINITY);
+      if (try_fast) {
+        float rsum[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) rsum[i] = 0.0f;
-          const float neg = -m_run;
+        for (int i = 0; i < 8; ++i) rsum[i] = 0.0f;
+        const uint64_t sc2 = f2_pack(prm.scale_log2, prm.scale_log2);
+        const uint64_t ng2 = f2_pack(-m_run, -m_run);
+        // two keys per packed fma / add; sums in 8 partial accumulators
 #pragma unroll
-          for (int c = 0; c < kBN; ++c) {
-            const float pv = fast_exp2(fmaf(SV(c), prm.scale_log2, neg));
-            sr[c >> 5][c & 31] = __float_as_uint(pv);
-            rsum[c & 7] += pv;
-          }
-          rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) + ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
-          if (__all_sync(0xffffffffu, rs <= 18446744073709551616.0f)) {  // 2^64; false for NaN
-            done = true;
-          } else {
+        for (int c = 0; c < kBN; c += 2) {
+          float x0, x1;
+          f2_unpack(ffma2(f2_pack(SV(c), SV(c + 1)), sc2, ng2), x0, x1);
+          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+          sr[c >> 5][c & 31] = __float_as_uint(p0);
+          sr[c >> 5][(c + 1) & 31] = __float_as_uint(p1);
+          const int a = (c >> 1) & 3;
+          uint64_t acc = f2_pack(rsum[a], rsum[4 + a]);
+          f2_unpack(fadd2(acc, f2_pack(p0, p1)), rsum[a], rsum[4 + a]);
+        }
+        rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) + ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
+        if (__all_sync(0xffffffffu, rs <= 18446744073709551616.0f)) {  // 2^64; false for NaN
+          done = true;
+        } else {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_addr + s_col + c * 32, sr[c]);
+          for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_addr + s_col + c * 32, sr[c]);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
-          }
+          for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
         }
       }
       if (!done) {
@@ -592,11 +600,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           if (!masked_tile) {
+            const uint64_t sc2 = f2_pack(prm.scale_log2, prm.scale_log2), ng2 = f2_pack(neg, neg);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float pv = fast_exp2(fmaf(__uint_as_float(sr[c][i]), prm.scale_log2, neg));
-              sr[c][i] = __float_as_uint(pv);
-              rsum[i & 7] += pv;
+            for (int i = 0; i < 32; i += 2) {
+              float x0, x1;
+              f2_unpack(ffma2(f2_pack(__uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1])), sc2, ng2), x0, x1);
+              const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              sr[c][i] = __float_as_uint(p0);
+              sr[c][i + 1] = __float_as_uint(p1);
+              const int a = (i >> 1) & 3;
+              uint64_t acc = f2_pack(rsum[a], rsum[4 + a]);
+              f2_unpack(fadd2(acc, f2_pack(p0, p1)), rsum[a], rsum[4 + a]);
             }
           } else {
 #pragma unroll

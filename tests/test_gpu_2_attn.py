@@ -98,6 +98,33 @@ def test_fully_masked_rows_and_empty_keys(dtype):
     assert torch.all(o == 0) and torch.all(torch.isneginf(l))
 
 
+@pytest.mark.parametrize("D,gain", [(64, 40.0), (128, 40.0), (64, 6.0), (128, 6.0)])
+def test_score_jump_after_the_first_tile(D, gain):
+    """Keys of later tiles scaled up so their scores exceed the first tile's
+    by tens (gain 6) to hundreds (gain 40) of log2 units: the kernel's
+    exponentials against the running reference overflow (to beyond 2^64, or
+    to +inf), and its fallback (S reloaded, or recomputed from Q and K in
+    shared memory when S's columns are already reused) must still give the
+    softmax of the definition."""
+    inp = workloads.make_attn(2, 4, 2, 300, 700, D, dtype=torch.bfloat16, n_pad=[0, 37], seed=41)
+    k = inp.k.float()
+    k[:, :, 128:384] *= gain  # tiles 1 and 2
+    k[:, 1, 600:] *= gain  # and a late tile of one head
+    inp.k = k.to(torch.bfloat16)
+    o, l = _run(inp)
+    ro, rl = oracle.attn(inp.q, inp.k, inp.v, inp.mask, inp.scale)
+    g = o.float().cpu().numpy()
+    assert np.all(np.isfinite(g))
+    # Such peaked rows return nearly one V row, up to |v| ~ 4.7, where bf16's
+    # own rounding of the output (half an ulp, 2^-9 relative) plus that of P
+    # (2^-9 of |v|) can pass 2e-2 on their own: the bound grows with |ref|
+    # by 2^-8, which a wrong fallback (wrong weights, O(1) errors) still fails.
+    err = np.abs(g - ro)
+    assert np.all(err <= 2e-2 + np.abs(ro) / 256), f"jump D={D} gain={gain}: max abs err {err.max():.3g}"
+    assert err.mean() <= 2e-3 + np.abs(ro).mean() / 256
+    assert_lse_close(l, rl, what=f"jump lse D={D} gain={gain}")
+
+
 def test_patch_small_workload_full():
     """B1 H16 P1944 D64 bf16 with a seeded 0-64 padded tail: every element."""
     inp = workloads.make_attn_inputs(workloads.ATTN_CONFIGS["patch_small"], seed=0)
