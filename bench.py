@@ -190,7 +190,10 @@ class Step:
         self.l_o = torch.empty_like(self.l_q)
         self.l_l = torch.empty(self.l_q.shape[:3], dtype=torch.float32, device=dev)
         self.d_o = torch.empty_like(self.dq)
-        self.ws_attn = lib.Workspace(256, device=dev)
+        # attention workspace: status word + per-tile key bounds, sized for the largest call
+        ws_need = max(lib.attn_fwd_workspace_size_for(x.cfg.B, x.cfg.Hkv, x.cfg.Pk, x.cfg.D)
+                      for x in (self.small, self.chunk, self.large))
+        self.ws_attn = lib.Workspace(ws_need, device=dev)
         self.ws_dec = lib.Workspace(lib.paged_decode_workspace_size(d.cfg.B, d.cfg.Hq, self.bt.shape[1], 16,
                                                                     d.cfg.D), device=dev)
         # algorithmic work
@@ -205,7 +208,8 @@ class Step:
         self.decode_bytes = (self.kv_bytes + 2 * d.cfg.B * d.cfg.Hq * d.cfg.D * 2 +
                              int(((d.ctx_lens.to(torch.int64) + 15) // 16).sum()) * 4)
         self.merge_bytes = 3 * T * H * D * 2 + 3 * H * T * 4
-        self.launches_per_step = 8  # attn x4, append, decode split + reduce, merge
+        # attn x4 (+ the key-bound pass of the two D=64 calls), append, decode split + reduce, merge
+        self.launches_per_step = 10
 
     @property
     def step_flops(self):

@@ -77,6 +77,7 @@ def load(build_if_missing: bool = False):
             "attn_version": (I32, []),
             "attn_status_string": (ctypes.c_char_p, [I32]),
             "attn_fwd_workspace_size": (SZ, []),
+            "attn_fwd_workspace_size_for": (SZ, [I32, I32, I64, I32]),
             "kv_append_workspace_size": (SZ, []),
             "paged_decode_workspace_size": (SZ, [I32, I32, I32, I32, I32]),
             "attn_fwd": (I32, [T, T, T, P, I64, F, T, P, P, SZ, P]),
@@ -106,7 +107,8 @@ def exported_symbols() -> list[str]:
             "attn_fwd_workspace_size", "kv_append_workspace_size", "paged_decode_workspace_size",
             "attn_check_device_status", "attn_reset_device_status", "attn_status_string", "attn_version",
             "paged_decode_attn_noalloc", "attn_selftest_wait_timeout", "attn_fwd_varlen",
-            "attn_key_padding_to_additive", "paged_decode_attn_append", "paged_prefill_attn"]
+            "attn_key_padding_to_additive", "paged_decode_attn_append", "paged_prefill_attn",
+            "attn_fwd_workspace_size_for"]
 
 
 # --------------------------------------------------------------------------
@@ -182,6 +184,18 @@ def _small_ws(device) -> Workspace:
     return ws
 
 
+def _attn_ws(q: torch.Tensor, k: torch.Tensor) -> Workspace:
+    """Default attn_fwd workspace: the status word plus room for the per-tile
+    key bounds of this shape (kept per device, grown when a call needs more)."""
+    need = attn_fwd_workspace_size_for(k.shape[0], k.shape[1], k.shape[2], k.shape[3])
+    key = ("attn", torch.device(q.device).index)
+    ws = _default_ws.get(key)
+    if ws is None or ws.nbytes < need:
+        ws = Workspace(max(need, 256), device=q.device)
+        _default_ws[key] = ws
+    return ws
+
+
 def check_device_status(ws: Workspace, stream=None) -> int:
     raw = ctypes.c_uint32(0)
     st = load().attn_check_device_status(ws.ptr, ctypes.byref(raw), _stream(stream))
@@ -190,6 +204,10 @@ def check_device_status(ws: Workspace, stream=None) -> int:
 
 def attn_fwd_workspace_size() -> int:
     return int(load().attn_fwd_workspace_size())
+
+
+def attn_fwd_workspace_size_for(batch: int, kv_heads: int, num_keys: int, head_dim: int) -> int:
+    return int(load().attn_fwd_workspace_size_for(batch, kv_heads, num_keys, head_dim))
 
 
 def paged_decode_workspace_size(batch: int, num_q_heads: int, max_blocks: int, block_size: int = 16,
@@ -220,7 +238,7 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, key_pad_mask: Op
     if key_pad_mask is not None:
         assert key_pad_mask.dtype == torch.float32 and key_pad_mask.stride(-1) == 1
         mptr, mstride = key_pad_mask.data_ptr(), key_pad_mask.stride(0)
-    ws = workspace or _small_ws(q.device)
+    ws = workspace or _attn_ws(q, k)
     dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
     st = lib.attn_fwd(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), mptr, mstride, float(scale),
                       ctypes.byref(do), _ptr(lse), ws.ptr, ws.nbytes, _stream(stream))
@@ -242,7 +260,7 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, key_lens:
         out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
     if lse is None and return_lse:
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
-    ws = workspace or _small_ws(q.device)
+    ws = workspace or _attn_ws(q, k)
     dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
     st = lib.attn_fwd_varlen(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), key_lens.data_ptr(), float(scale),
                              ctypes.byref(do), _ptr(lse), ws.ptr, ws.nbytes, _stream(stream))

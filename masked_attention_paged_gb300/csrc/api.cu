@@ -107,6 +107,14 @@ const char* attn_status_string(attn_status s) {
 }
 
 size_t attn_fwd_workspace_size(void) { return kStatusBytes; }
+
+size_t attn_fwd_workspace_size_for(int32_t batch, int32_t kv_heads, int64_t num_keys, int32_t head_dim) {
+  if (batch < 0 || kv_heads < 0 || num_keys < 0 || head_dim <= 0) return 0;
+  if (head_dim != 64) return kStatusBytes;  // the key-tile bounds serve the D = 64 kernel only
+  const size_t tiles = static_cast<size_t>((num_keys + kKeyTile - 1) / kKeyTile);
+  const size_t bytes = static_cast<size_t>(batch) * kv_heads * tiles * sizeof(float);
+  return kStatusBytes + ((bytes + 255) & ~size_t(255));
+}
 size_t kv_append_workspace_size(void) { return kStatusBytes; }
 
 size_t paged_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t max_blocks, int32_t block_size,
@@ -148,6 +156,7 @@ static attn_status attn_fwd_impl(const attn_tensor* q, const attn_tensor* k, con
   a.mask = key_pad_mask;
   a.mask_stride = mask_stride_b;
   a.key_lens = key_lens;
+  a.key_bound = nullptr;
   a.scale = scale;
   a.lse = lse;
   a.status = static_cast<uint32_t*>(workspace);
@@ -156,6 +165,17 @@ static attn_status attn_fwd_impl(const attn_tensor* q, const attn_tensor* k, con
   if (q->dtype == ATTN_BF16) {
     if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
     if (!vec16_ok(q) || !vec16_ok(k) || !vec16_ok(v)) return ATTN_ERR_INVALID_ARG;
+    // D = 64 with room in the workspace: per-tile key bounds first, which
+    // let the kernel skip its softmax max pass on most tiles.  The extra pass
+    // (one read of K and a launch) pays only on calls of a few hundred
+    // microseconds and up: from B Hq Pq Pk D = 2^36 on.
+    const double work = static_cast<double>(B) * Hq * static_cast<double>(Pq) * static_cast<double>(Pk) * D;
+    if (D == 64 && work >= 68719476736.0 &&
+        workspace_bytes >= attn_fwd_workspace_size_for(static_cast<int32_t>(B), static_cast<int32_t>(Hkv), Pk,
+                                                       static_cast<int32_t>(D))) {
+      a.key_bound = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
+      if ((st = from_cuda(launch_key_tile_bound(a, stream))) != ATTN_OK) return st;
+    }
     return from_cuda(launch_attn_fwd_tc(a, stream));
   }
   if (D > 128 || D % 4 != 0) return ATTN_ERR_UNSUPPORTED;

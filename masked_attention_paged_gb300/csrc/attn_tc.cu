@@ -104,6 +104,7 @@ struct Barriers {
   uint64_t m_full[2], m_empty[2];  // mask tile staging (warp 2 -> softmax warps)
   uint64_t o_final[2];
   int m_flag[2];                   // tile has a masked key (or keys past Pk)
+  float kmax[2];                   // largest |k| element of the tile (score bound)
   uint32_t tmem_base;
   int abort;
 };
@@ -122,6 +123,8 @@ struct TcParams {
   const float* mask;
   int64_t mask_stride;
   const int32_t* key_lens;  // per-batch valid keys, or null (all Pk)
+  const float* key_bound;   // [B, Hkv, key_tiles] largest |k| element per 128-key tile, or null
+  int key_tiles;
   // PAGED: cache read through the block table
   const int32_t* bt;
   int64_t bt_stride;
@@ -147,6 +150,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
   using C = Cfg<D>;
+  // With P apart from S the softmax skips the max pass on tiles where a
+  // bound certifies that no exponential can overflow (see the stager)
+  constexpr bool kCert = C::kSepP && !PAGED;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Barriers* bars = reinterpret_cast<Barriers*>(smem + C::kOffBar);
@@ -446,6 +452,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<float4*>(mbuf + s * kBN + lane * 4) = make_float4(v[0], v[1], v[2], v[3]);
       any = __any_sync(0xffffffffu, any);
       if (lane == 0) bars->m_flag[s] = any || !prm.scale_positive;
+      if constexpr (kCert) {
+        // The largest |k| element of K_j, precomputed (+inf without it):
+        // every score of the tile obeys |q.k| <= |q|_1 max|k|, which lets the
+        // softmax skip its max pass.
+        if (lane == 0)
+          bars->kmax[s] = prm.key_bound != nullptr
+                              ? prm.key_bound[(static_cast<int64_t>(b) * (prm.Hq / prm.group) + g) * prm.key_tiles + j]
+                              : INFINITY;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->m_full[s]);
     }
@@ -465,6 +480,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = -INFINITY;  // reference max, log2 units
     float l_run = 0.0f;       // running sum of 2^(x - m_run)
     bool ok = true;
+    // kCert: L1 norm of this row's query (rows past Pq were zero-filled)
+    float q_l1 = 0.0f;
+    if constexpr (kCert) {
+      if (nkv > 0 && __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, abort, prm.status))) {
+        const uint8_t* qt = smem + C::kOffQ + t * C::kTileBytes;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {  // 128-byte swizzled row: chunk ch sits at ch ^ (row % 8)
+          const uint4 w = *reinterpret_cast<const uint4*>(qt + row * 128 + ((ch ^ (row & 7)) << 4));
+          q_l1 += (fabsf(bf16lo_to_f32(w.x)) + fabsf(bf16hi_to_f32(w.x))) +
+                  (fabsf(bf16lo_to_f32(w.y)) + fabsf(bf16hi_to_f32(w.y))) +
+                  (fabsf(bf16lo_to_f32(w.z)) + fabsf(bf16hi_to_f32(w.z))) +
+                  (fabsf(bf16lo_to_f32(w.w)) + fabsf(bf16hi_to_f32(w.w)));
+        }
+      }
+    }
     // PAGED: keys [0, row_lim) are this row's (its own position when causal)
     int row_lim = n_keys;
     if constexpr (PAGED) {
@@ -499,14 +529,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       float alpha = 1.0f;
       float rs = 0.0f;
       bool done = false;
-      // Fast path (P over S only): exponentiate against the current reference
-      // max without a max pass.  Every term is <= 2^64 exactly when the row
-      // sum is, which keeps the sums far from fp32 overflow; if some row
-      // fails, the warp reloads S (its columns are intact until P is written
-      // over them) and takes the full path below.  With P apart from S, S's
-      // columns are handed back right after the load, which is worth more
-      // than skipping the max pass.
-      const bool try_fast = !C::kSepP && !masked_tile && __all_sync(0xffffffffu, m_run != -INFINITY);
+      // Fast path: exponentiate against the current reference max without a
+      // max pass.  P over S: every term is <= 2^64 exactly when the row sum
+      // is, which keeps the sums far from fp32 overflow; if some row fails,
+      // the warp reloads S (its columns are intact until P is written over
+      // them) and takes the full path below.  P apart from S (S's columns are
+      // handed back right after the load, so nothing could be reloaded): the
+      // path is taken only where |s| <= |q|_1 max|k| certifies every term to
+      // be <= 2^60.
+      bool try_fast;
+      if constexpr (kCert) {
+        const float bound = q_l1 * bars->kmax[mb_i] * prm.scale_log2;  // scale > 0 on unmasked tiles
+        try_fast = !masked_tile && __all_sync(0xffffffffu, m_run != -INFINITY && bound - m_run <= 60.0f);
+      } else {
+        try_fast = !C::kSepP && !masked_tile && __all_sync(0xffffffffu, m_run != -INFINITY);
+      }
       if (try_fast) {
         float rsum[8];
 #pragma unroll
@@ -526,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           f2_unpack(fadd2(acc, f2_pack(p0, p1)), rsum[a], rsum[4 + a]);
         }
         rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) + ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
-        if (__all_sync(0xffffffffu, rs <= 18446744073709551616.0f)) {  // 2^64; false for NaN
+        if (kCert || __all_sync(0xffffffffu, rs <= 18446744073709551616.0f)) {  // 2^64; false for NaN
           done = true;
         } else {
 #pragma unroll
@@ -634,7 +671,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 4; ++c) chunk_out(c);
         }
       } else {
-        // fast path passed its check: now P may overwrite S's columns
+        // fast path passed: now P may be written (over S's columns, or into
+        // P's own columns once PV_t(j-1) has read them)
+        if constexpr (C::kSepP) {
+          if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], (j - 1) & 1, abort, prm.status))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pw[16];
@@ -844,6 +889,8 @@ cudaError_t launch_tc(const AttnFwdArgs& a, cudaStream_t stream) {
   p.mask = a.mask;
   p.mask_stride = a.mask_stride;
   p.key_lens = a.key_lens;
+  p.key_bound = a.key_bound;
+  p.key_tiles = static_cast<int>((a.Pk + kBN - 1) / kBN);
   p.out = a.out.data;
   p.out_stride[0] = a.out.stride[0];
   p.out_stride[1] = a.out.stride[1];

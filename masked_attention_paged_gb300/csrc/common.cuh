@@ -69,6 +69,13 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// Elementwise max of a bf16 pair and the absolute values of another.
+__device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t acc, uint32_t w) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(acc), "r"(w & 0x7fff7fffu));
+  return d;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -22,6 +22,7 @@ struct AttnFwdArgs {
   const float* mask;  // [B, Pk] additive, row stride mask_stride; may be null
   int64_t mask_stride;
   const int32_t* key_lens;  // [B] valid keys per batch row (keys past it are padding); may be null
+  float* key_bound;         // [B, Hkv, ceil(Pk/128)] largest |k| element per key tile, or null
   float scale;
   float* lse;         // [B, Hq, Pq] contiguous, may be null
   uint32_t* status;   // device status word
@@ -33,6 +34,9 @@ cudaError_t launch_attn_fwd_tc(const AttnFwdArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_fwd_simt(const AttnFwdArgs& a, cudaStream_t stream);
 // Pk == 0: out = 0, lse = -inf
 cudaError_t launch_attn_empty_keys(const AttnFwdArgs& a, cudaStream_t stream);
+// a.key_bound[(b * Hkv + g) * tiles + j] = max |k| over keys [128 j, 128 j + 128) of (b, g)
+cudaError_t launch_key_tile_bound(const AttnFwdArgs& a, cudaStream_t stream);
+constexpr int kKeyTile = 128;  // keys per tile of the tensor-core kernel
 
 struct MergeArgs {
   int n;

@@ -433,6 +433,48 @@ __global__ void padding_mask_to_additive_kernel(const uint8_t* kpm, int64_t kpm_
 }
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// key_tile_bound: the largest |k| element of each 128-key tile of bf16 K,
+// one CTA per (tile, KV head, batch), 16-byte loads.
+// ---------------------------------------------------------------------------
+namespace {
+__global__ void key_tile_bound_kernel(const uint16_t* __restrict__ k, int64_t s0, int64_t s1, int64_t s2, int Pk,
+                                      int D, int Hkv, int tiles, float* __restrict__ bound) {
+  const int j = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int key0 = j * kKeyTile;
+  const int nkeys = min(kKeyTile, Pk - key0);
+  const int vpr = D / 8;
+  uint32_t mx2 = 0u;
+  for (int i = threadIdx.x; i < nkeys * vpr; i += blockDim.x) {
+    const int key = key0 + i / vpr, c = i % vpr;
+    const uint4 w = *reinterpret_cast<const uint4*>(k + b * s0 + g * s1 + static_cast<int64_t>(key) * s2 + c * 8);
+    mx2 = bf16x2_max_abs(mx2, w.x);
+    mx2 = bf16x2_max_abs(mx2, w.y);
+    mx2 = bf16x2_max_abs(mx2, w.z);
+    mx2 = bf16x2_max_abs(mx2, w.w);
+  }
+  float m = fmaxf(bf16lo_to_f32(mx2), bf16hi_to_f32(mx2));
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __shared__ float part[8];
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) m = fmaxf(m, part[w]);
+    bound[(static_cast<int64_t>(b) * Hkv + g) * tiles + j] = m;
+  }
+}
+}  // namespace
+
+cudaError_t launch_key_tile_bound(const AttnFwdArgs& a, cudaStream_t stream) {
+  const int tiles = static_cast<int>((a.Pk + kKeyTile - 1) / kKeyTile);
+  dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(a.Hkv), static_cast<unsigned>(a.B));
+  key_tile_bound_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(a.k.data), a.k.stride[0],
+                                                  a.k.stride[1], a.k.stride[2], static_cast<int>(a.Pk),
+                                                  static_cast<int>(a.D), static_cast<int>(a.Hkv), tiles,
+                                                  a.key_bound);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_padding_mask_to_additive(const uint8_t* kpm, int64_t kpm_stride, int64_t B, int64_t Pk,
                                             float* out, int64_t out_stride, cudaStream_t stream) {
   const int64_t blocks = (Pk + 255) / 256;

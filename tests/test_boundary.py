@@ -58,6 +58,11 @@ def test_status_strings_and_version(L):
 
 def test_workspace_sizes(L):
     assert L.attn_fwd_workspace_size() == 256
+    # with the per-tile key bounds: one float per (batch, KV head, 128-key tile), D = 64 only
+    assert L.attn_fwd_workspace_size_for(1, 16, 32000, 64) == 256 + (16 * 250 * 4 + 255) // 256 * 256
+    assert L.attn_fwd_workspace_size_for(2, 4, 129, 64) == 256 + 256
+    assert L.attn_fwd_workspace_size_for(1, 24, 16380, 128) == 256
+    assert L.attn_fwd_workspace_size_for(1, 16, -1, 64) == 0
     assert L.kv_append_workspace_size() == 256
     # decode: status block + partials [B, Hq, n_split, D] + lse [B, Hq, n_split], split = 1024 tokens
     n_split = -(-513 * 16 // 1024)

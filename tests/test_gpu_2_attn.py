@@ -18,13 +18,17 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _run(inp, out_dtype=None):
+def _run(inp, out_dtype=None, bounds=False):
+    """attn_fwd on the GPU; bounds=True gives it the workspace with room for
+    the per-tile key bounds (the D = 64 kernel then skips its max pass where
+    they rule out overflow), False the bare status word."""
     q, k, v = inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV)
     mask = inp.mask.to(DEV) if inp.mask is not None else None
     out = None
     if out_dtype is not None:
         out = torch.empty(q.shape, dtype=out_dtype, device=DEV)
-    ws = lib.Workspace(256)
+    B, Hkv, Pk, D = k.shape
+    ws = lib.Workspace(lib.attn_fwd_workspace_size_for(B, Hkv, Pk, D) if bounds else 256)
     o, l = lib.attn_fwd(q, k, v, mask, inp.scale, out=out, workspace=ws)
     assert ws.status() == 0
     return o, l
@@ -62,9 +66,10 @@ def test_f32_small_shapes(B, Hq, Hkv, Pq, Pk, D, pad):
     (1, 2, 2, 513, 257, 128, [0]),      # Pq > Pk
     (3, 2, 1, 64, 700, 128, [1, 128, 300]),
 ])
-def test_bf16_tensor_core_small_shapes(B, Hq, Hkv, Pq, Pk, D, pad):
+@pytest.mark.parametrize("bounds", [False, True])
+def test_bf16_tensor_core_small_shapes(B, Hq, Hkv, Pq, Pk, D, pad, bounds):
     inp = workloads.make_attn(B, Hq, Hkv, Pq, Pk, D, dtype=torch.bfloat16, n_pad=pad, seed=2)
-    o, l = _run(inp)
+    o, l = _run(inp, bounds=bounds)
     ro, rl = oracle.attn(inp.q, inp.k, inp.v, inp.mask, inp.scale)
     assert_out_close(o, ro)
     assert_lse_close(l, rl)
@@ -98,8 +103,9 @@ def test_fully_masked_rows_and_empty_keys(dtype):
     assert torch.all(o == 0) and torch.all(torch.isneginf(l))
 
 
-@pytest.mark.parametrize("D,gain", [(64, 40.0), (128, 40.0), (64, 6.0), (128, 6.0)])
-def test_score_jump_after_the_first_tile(D, gain):
+@pytest.mark.parametrize("bounds", [False, True])
+@pytest.mark.parametrize("D,gain", [(64, 40.0), (128, 40.0), (64, 6.0), (128, 6.0), (64, 2.5)])
+def test_score_jump_after_the_first_tile(D, gain, bounds):
     """Keys of later tiles scaled up so their scores exceed the first tile's
     by tens (gain 6) to hundreds (gain 40) of log2 units: the kernel's
     exponentials against the running reference overflow (to beyond 2^64, or
@@ -111,7 +117,7 @@ def test_score_jump_after_the_first_tile(D, gain):
     k[:, :, 128:384] *= gain  # tiles 1 and 2
     k[:, 1, 600:] *= gain  # and a late tile of one head
     inp.k = k.to(torch.bfloat16)
-    o, l = _run(inp)
+    o, l = _run(inp, bounds=bounds)
     ro, rl = oracle.attn(inp.q, inp.k, inp.v, inp.mask, inp.scale)
     g = o.float().cpu().numpy()
     assert np.all(np.isfinite(g))
@@ -125,10 +131,30 @@ def test_score_jump_after_the_first_tile(D, gain):
     assert_lse_close(l, rl, what=f"jump lse D={D} gain={gain}")
 
 
+@pytest.mark.parametrize("gain", [1.0, 3.0, 8.0])
+def test_key_bound_path_at_its_threshold(gain):
+    """D = 64 at the size where attn_fwd starts using the per-tile key bounds
+    (B Hq Pq Pk D = 2^36): the bound-certified tiles skip the max pass, the
+    rest (later tiles' keys scaled by `gain`, and the padded tail) take the
+    full path; sampled rows of every head against the oracle."""
+    inp = workloads.make_attn(1, 16, 8, 8192, 8192, 64, dtype=torch.bfloat16, n_pad=300, seed=43)
+    k = inp.k.float()
+    k[:, :, 4096:] *= gain
+    inp.k = k.to(torch.bfloat16)
+    o, l = _run(inp, bounds=True)
+    rows = sample_rows(1, 16, 8192, 64, seed=12)
+    ro, rl = oracle.attn(inp.q, inp.k, inp.v, inp.mask, inp.scale, rows=rows)
+    g = o.reshape(-1, 64)[torch.from_numpy(rows).to(DEV)].float().cpu().numpy()
+    err = np.abs(g - ro)
+    assert np.all(np.isfinite(g))
+    assert np.all(err <= 2e-2 + np.abs(ro) / 256), f"gain {gain}: max abs err {err.max():.3g}"
+    assert_lse_close(l.reshape(-1)[torch.from_numpy(rows).to(DEV)], rl)
+
+
 def test_patch_small_workload_full():
     """B1 H16 P1944 D64 bf16 with a seeded 0-64 padded tail: every element."""
     inp = workloads.make_attn_inputs(workloads.ATTN_CONFIGS["patch_small"], seed=0)
-    o, l = _run(inp)
+    o, l = _run(inp, bounds=True)  # the workspace bench.py gives it
     ro, rl = oracle.attn(inp.q, inp.k, inp.v, inp.mask, inp.scale)
     assert_out_close(o, ro)
     assert_lse_close(l, rl)
@@ -137,7 +163,7 @@ def test_patch_small_workload_full():
 def test_patch_large_workload_sampled():
     """B1 H16 P32000 D64 bf16, last 128 keys padded: 96 seeded query rows."""
     inp = workloads.make_attn_inputs(workloads.ATTN_CONFIGS["patch_large"], seed=0)
-    o, l = _run(inp)
+    o, l = _run(inp, bounds=True)  # the workspace bench.py gives it
     rows = sample_rows(1, 16, 32000, 96, seed=11)
     ro, rl = oracle.attn(inp.q, inp.k, inp.v, inp.mask, inp.scale, rows=rows)
     assert_out_close(o.reshape(-1, 64)[torch.from_numpy(rows).to(DEV)], ro)
