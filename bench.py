@@ -388,7 +388,7 @@ def next_rows(step, K, W, pk):
         "paged_prefill_attn": {"workload": "prefill_chunk (16 seqs x 1024-token causal chunk after U[0, 7168] "
                                            "cached, Hq 32, Hkv 8, D 128)",
                                "ms": p_ms, "tflops": p_tf, "frac": p_tf / peak_t, "launches": 2,
-                               "flops": p_flops},
+                               "flops": p_flops, "traffic": traffic("attn_fwd_tc_kernel_paged_prefill")},
     }
 
 
@@ -502,7 +502,8 @@ def main():
         "attn_fwd": {"ms": attn_ms, "tflops": attn_tflops, "frac": attn_tflops / peak_t,
                      "patch_small_tflops": step.flops_small / (seg["attn_small"] * 1e-3) / 1e12,
                      "chunk_tflops": step.flops_chunk / (seg["attn_chunks"] * 1e-3) / 1e12,
-                     "patch_large_tflops": step.flops_large / (seg["attn_large"] * 1e-3) / 1e12},
+                     "patch_large_tflops": step.flops_large / (seg["attn_large"] * 1e-3) / 1e12,
+                     "patch_large_traffic": traffic("attn_fwd_tc_kernel_patch_large")},
         "paged_decode_attn": {"ms": seg["decode"], "kv_gbs": step.kv_bytes / (seg["decode"] * 1e-3) / 1e9,
                               "gbs": dec_gbs, "frac": dec_gbs / pk["hbm_gbs"]},
         "kv_append": {"ms": seg["append"]},
