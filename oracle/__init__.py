@@ -20,6 +20,8 @@ Sources, by page title and section:
   token = layers x 2 x H_KV x D_head x B_elem.
 * decode -- "KV cache in nanoVLM" (how KV caching optimises inference): the
   new token's K/V is appended to the cache and its query attends over it.
+* INT8 KV -- "LLM inference memory accounting" (section 18): codes plus a
+  float32 scale per token row; attention runs on the dequantised values.
 * prefill -- "KV cache in nanoVLM" (prefill and decode phases) and "LLM
   inference memory accounting" (section 20, chunked prefill): a prompt or a
   chunk of it is processed in one pass, its K/V written to the cache; a
@@ -326,6 +328,70 @@ def paged_prefill(q, k_cache, v_cache, block_table, start_pos, causal: bool, sca
         raise ValueError("oracle_paged_prefill: block table entry outside the cache "
                          "or sequence longer than the table")
     return out, lse
+
+
+# --------------------------------------------------------------------------
+# INT8 KV ("LLM inference memory accounting", section 18: BF16 KV to INT8
+# halves the payload and adds scale metadata and a dequantisation step)
+# --------------------------------------------------------------------------
+def quantize_rows_q8(x):
+    """Symmetric INT8 code of each row (last axis) with one float32 scale per
+    row, every step in float32 as written:
+        a     = max_d |x_d|
+        scale = a / 127                      (0 for an all-zero row)
+        q_d   = clamp(rint(x_d / scale), -127, 127)   (0 when scale is 0)
+    rint rounds half to even.  Returns (int8 codes, float32 scales)."""
+    import torch
+    xs = np.asarray(x.detach().cpu().to(torch.float32).numpy() if hasattr(x, "detach") else x, dtype=np.float32)
+    a = np.max(np.abs(xs), axis=-1)
+    scale = (a / np.float32(127.0)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0)).astype(np.float32)
+    q = np.rint(xs / safe[..., None]).astype(np.float32)
+    q = np.clip(q, -127, 127)
+    q = np.where(scale[..., None] > 0, q, 0).astype(np.int8)
+    return q, scale
+
+
+def dequantize_rows_q8(q, scale):
+    """x_hat = q * scale in float32 (exact in float64 afterwards)."""
+    return (np.asarray(q, dtype=np.float32) * np.asarray(scale, dtype=np.float32)[..., None]).astype(np.float32)
+
+
+def kv_append_q8(kq_cache, vq_cache, k_scale, v_scale, block_table, pos, k_new, v_new, block_size: int = 16):
+    """Expected INT8 caches after appending one token per sequence: the new
+    token's K and V rows (per KV head) are quantised with quantize_rows_q8 and
+    written, codes and scales, to block block_table[b, pos // block_size],
+    slot pos % block_size; pos < 0 skips the sequence.  Caches
+    [num_blocks, Hkv, block_size, D] int8, scales [num_blocks, Hkv,
+    block_size] float32.  Returns numpy copies (kq, vq, k_scale, v_scale)."""
+    kq = np.array(_np(kq_cache), dtype=np.int8, copy=True)
+    vq = np.array(_np(vq_cache), dtype=np.int8, copy=True)
+    ks = np.array(_np(k_scale), dtype=np.float32, copy=True)
+    vs = np.array(_np(v_scale), dtype=np.float32, copy=True)
+    bt = np.asarray(_np(block_table), dtype=np.int64)
+    ps = np.asarray(_np(pos), dtype=np.int64)
+    qk, sk = quantize_rows_q8(k_new)
+    qv, sv = quantize_rows_q8(v_new)
+    for b in range(ps.shape[0]):
+        if ps[b] < 0:
+            continue
+        blk = bt[b, ps[b] // block_size]
+        slot = ps[b] % block_size
+        kq[blk, :, slot, :] = qk[b]
+        vq[blk, :, slot, :] = qv[b]
+        ks[blk, :, slot] = sk[b]
+        vs[blk, :, slot] = sv[b]
+    return kq, vq, ks, vs
+
+
+def paged_decode_q8(q, kq_cache, vq_cache, k_scale, v_scale, block_table, ctx_lens, scale: Optional[float] = None,
+                    block_size: int = 16):
+    """Paged decode over an INT8 cache: the definition of paged_decode applied
+    to the dequantised K and V (q * scale, float32, exact in float64)."""
+    import torch
+    kd = torch.from_numpy(dequantize_rows_q8(_np(kq_cache), _np(k_scale)))
+    vd = torch.from_numpy(dequantize_rows_q8(_np(vq_cache), _np(v_scale)))
+    return paged_decode(q, kd, vd, block_table, ctx_lens, scale, block_size)
 
 
 # --------------------------------------------------------------------------

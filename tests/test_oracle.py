@@ -470,6 +470,129 @@ def test_prefill_rows_match_decode_and_contiguous_attention():
 
 
 # --------------------------------------------------------------------------
+# INT8 KV
+# --------------------------------------------------------------------------
+def _check_q8_pins(quant):
+    """The quantiser pins, against any candidate implementation `quant`."""
+    g = torch.Generator().manual_seed(13)
+    x = torch.randn(6, 4, 128, generator=g).to(torch.bfloat16)
+    x[0, 0] = 0.0  # an all-zero row
+    q, s = quant(x)
+    xf = x.float().numpy()
+    assert q.dtype == np.int8 and np.abs(q.astype(np.int32)).max() <= 127
+    # the largest |x| of a row maps to +-127 exactly, and the zero row to 0 / 0
+    am = np.abs(xf).argmax(-1)
+    for i in range(6):
+        for h in range(4):
+            if i == 0 and h == 0:
+                assert s[i, h] == 0 and not q[i, h].any()
+                continue
+            assert abs(int(q[i, h, am[i, h]])) == 127
+            assert np.sign(q[i, h, am[i, h]]) == np.sign(xf[i, h, am[i, h]])
+    # every element within half a step of its row's scale (plus the float32
+    # rounding of x / scale, < 1e-5 of a step for |x / scale| <= 127)
+    err = np.abs(q.astype(np.float64) * s[..., None].astype(np.float64) - xf)
+    assert np.all(err <= 0.5 * s[..., None].astype(np.float64) * (1 + 1e-4) + 1e-30)
+    # hand-computed: scale 127/127 = 1 and ties round half to even
+    t = torch.tensor([[[127.0, 0.5, 1.5, 2.5, -0.5, -3.5, 126.5, 0.0]]])
+    qt, st = quant(t)
+    assert float(st[0, 0]) == 1.0
+    assert qt[0, 0].tolist() == [127, 0, 2, 2, 0, -4, 126, 0]
+    # a row twice as large: the same codes and twice the scale (exact in binary)
+    q2, s2 = quant(x * 2)
+    np.testing.assert_array_equal(q2, q)
+    np.testing.assert_array_equal(s2, 2 * s)
+
+
+def test_q8_quantiser_pins():
+    _check_q8_pins(oracle.quantize_rows_q8)
+
+
+def test_q8_quantiser_matches_library_int8_quantisation():
+    """PyTorch's per-tensor qint8 quantiser with the same scale (it multiplies by
+    the reciprocal where the oracle divides, so codes may differ by one only
+    where x / scale lies within float rounding of a half)."""
+    g = torch.Generator().manual_seed(14)
+    x = torch.randn(64, 128, generator=g).to(torch.bfloat16)
+    q, s = oracle.quantize_rows_q8(x)
+    for r in range(64):
+        tq = torch.quantize_per_tensor(x[r].float(), float(s[r]), 0, torch.qint8).int_repr().numpy()
+        d = np.abs(tq.astype(np.int32) - q[r].astype(np.int32))
+        assert d.max() <= 1
+        ratio = x[r].float().numpy() / s[r]
+        assert np.all(np.abs(np.abs(ratio[d == 1] - np.floor(ratio[d == 1])) - 0.5) < 1e-4)
+
+
+def test_q8_planted_mistakes_are_caught():
+    def per_tensor(x):  # one scale for the whole tensor instead of one per row
+        xs = x.float().numpy()
+        s = np.float32(np.abs(xs).max() / np.float32(127))
+        q = np.clip(np.rint(xs / s), -127, 127).astype(np.int8)
+        return q, np.full(xs.shape[:-1], s, dtype=np.float32)
+    def scale_128(x):
+        xs = x.float().numpy()
+        s = (np.abs(xs).max(-1) / np.float32(128)).astype(np.float32)
+        q = np.clip(np.rint(xs / np.where(s > 0, s, 1)[..., None]), -127, 127).astype(np.int8)
+        return q, s
+    def truncate(x):
+        xs = x.float().numpy()
+        s = (np.abs(xs).max(-1) / np.float32(127)).astype(np.float32)
+        q = np.clip(np.trunc(xs / np.where(s > 0, s, 1)[..., None]), -127, 127).astype(np.int8)
+        return q, s
+    def half_up(x):
+        xs = x.float().numpy()
+        s = (np.abs(xs).max(-1) / np.float32(127)).astype(np.float32)
+        q = np.clip(np.floor(xs / np.where(s > 0, s, 1)[..., None] + 0.5), -127, 127).astype(np.int8)
+        return q, s
+    for bad in (per_tensor, scale_128, truncate, half_up):
+        with pytest.raises(AssertionError):
+            _check_q8_pins(bad)
+
+
+def test_q8_append_writes_one_quantised_row_per_head():
+    cfg = workloads.DecodeConfig("q", 5, 8, 2, 64, 16, 0, 100, 3)
+    d = workloads.make_decode_inputs_q8(cfg, seed=15, ctx=[0, 15, 16, 17, 100])
+    pos = d.pos.clone()
+    pos[3] = -1  # idle
+    kq, vq, ks, vs = oracle.kv_append_q8(d.kq_cache, d.vq_cache, d.k_scale, d.v_scale, d.block_table, pos,
+                                         d.k_new, d.v_new)
+    qk, sk = oracle.quantize_rows_q8(d.k_new)
+    changed = ((kq != d.kq_cache.numpy()).any(axis=(1, 3)) |
+               ~np.isclose(ks, d.k_scale.numpy(), equal_nan=True).all(axis=1))
+    for b in range(5):
+        if b == 3:
+            continue
+        blk, slot = int(d.block_table[b, int(pos[b]) // 16]), int(pos[b]) % 16
+        np.testing.assert_array_equal(kq[blk, :, slot], qk[b])
+        np.testing.assert_array_equal(ks[blk, :, slot], sk[b])
+        assert changed[blk, slot]
+        changed[blk, slot] = False
+    assert not changed.any()  # nothing else, and nothing for the idle sequence
+
+
+def test_q8_decode_on_exactly_representable_cache_equals_bf16_decode():
+    """Rows of integers times 1/4 with one element +-127/4: quantisation is
+    exact, so the INT8 decode equals the (pinned) bf16 decode on the same
+    values, to the last bit of fp64."""
+    cfg = workloads.DecodeConfig("q", 3, 8, 2, 64, 16, 0, 300, 2)
+    d = workloads.make_decode_inputs(cfg, seed=16, ctx=[10, 100, 300])
+    g = torch.Generator().manual_seed(17)
+    def exact_rows(shape):
+        v = torch.randint(-126, 127, shape, generator=g).float()
+        v[..., 0] = 127.0
+        return (v / 4).to(torch.bfloat16)
+    kc = exact_rows(d.k_cache.shape)
+    vc = exact_rows(d.v_cache.shape)
+    kq, ks = oracle.quantize_rows_q8(kc)
+    vq, vs = oracle.quantize_rows_q8(vc)
+    assert np.all(ks == 127 / 4 / 127) and np.all(vs == 0.25)
+    o8, l8 = oracle.paged_decode_q8(d.q, kq, vq, ks, vs, d.block_table, d.ctx, d.scale)
+    o, l = oracle.paged_decode(d.q, kc, vc, d.block_table, d.ctx, d.scale)
+    np.testing.assert_array_equal(o8, o)
+    np.testing.assert_array_equal(l8, l)
+
+
+# --------------------------------------------------------------------------
 # the pages' worked numbers
 # --------------------------------------------------------------------------
 def test_kv_bytes_per_token_worked_example():

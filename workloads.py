@@ -373,3 +373,77 @@ def prefill_flops(start_pos: torch.Tensor, T: int, Hq: int, D: int, causal: bool
     else:
         keys = ((st + T) * T).sum().item()
     return 4.0 * Hq * D * keys
+
+
+# --------------------------------------------------------------------------
+# Paged decode over an INT8 cache (codes and one float32 scale per token row)
+# --------------------------------------------------------------------------
+@dataclasses.dataclass
+class DecodeInputsQ8:
+    cfg: DecodeConfig
+    ctx: torch.Tensor
+    pos: torch.Tensor
+    ctx_lens: torch.Tensor
+    block_table: torch.Tensor
+    kq_cache: torch.Tensor  # int8 [num_blocks, Hkv, block_size, D]; 0 in unfilled slots
+    vq_cache: torch.Tensor
+    k_scale: torch.Tensor  # float32 [num_blocks, Hkv, block_size]; NaN in unfilled slots
+    v_scale: torch.Tensor
+    k_new: torch.Tensor  # bf16 [B, Hkv, D]
+    v_new: torch.Tensor
+    q: torch.Tensor  # bf16 [B, Hq, D]
+    scale: float
+
+    @property
+    def num_blocks(self) -> int:
+        return int(self.kq_cache.shape[0])
+
+
+def make_decode_inputs_q8(cfg: DecodeConfig, seed: int = 0, ctx: Optional[Sequence[int]] = None) -> DecodeInputsQ8:
+    """The decode workload's shapes and block assignment with an INT8 cache:
+    codes uniform in [-127, 127] and scales uniform in [0.01, 0.04] (rows of
+    N(0,1)-sized values) for slots holding one of the first ctx tokens; codes
+    0 and scale NaN everywhere else, so reading an unfilled slot shows."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    B, bs = cfg.B, cfg.block_size
+    if ctx is None:
+        ctx_t = torch.randint(cfg.ctx_lo, cfg.ctx_hi + 1, (B,), generator=g)
+    else:
+        ctx_t = torch.tensor(list(ctx), dtype=torch.int64)
+        assert ctx_t.numel() == B
+    lens = ctx_t + 1
+    nblk = (lens + bs - 1) // bs
+    width = max(cfg.max_blocks, int(nblk.max().item()))
+    n_phys = int(nblk.sum().item()) + cfg.spare_blocks
+    perm = torch.randperm(n_phys, generator=g)
+    bt = torch.full((B, width), -1, dtype=torch.int32)
+    off = 0
+    for b in range(B):
+        n = int(nblk[b])
+        bt[b, :n] = perm[off:off + n].to(torch.int32)
+        off += n
+    shape = (n_phys, cfg.Hkv, bs, cfg.D)
+    kq = torch.randint(-127, 128, shape, generator=g, dtype=torch.int32).to(torch.int8)
+    vq = torch.randint(-127, 128, shape, generator=g, dtype=torch.int32).to(torch.int8)
+    ks = 0.01 + 0.03 * torch.rand((n_phys, cfg.Hkv, bs), generator=g)
+    vs = 0.01 + 0.03 * torch.rand((n_phys, cfg.Hkv, bs), generator=g)
+    filled = torch.zeros(n_phys, bs, dtype=torch.bool)
+    for b in range(B):
+        t = torch.arange(int(ctx_t[b]))
+        filled[bt[b, (t // bs)].long(), t % bs] = True
+    hole = ~filled
+    kq.permute(0, 2, 1, 3)[hole] = 0
+    vq.permute(0, 2, 1, 3)[hole] = 0
+    ks.permute(0, 2, 1)[hole] = float("nan")
+    vs.permute(0, 2, 1)[hole] = float("nan")
+    k_new = _randn((B, cfg.Hkv, cfg.D), g, torch.bfloat16)
+    v_new = _randn((B, cfg.Hkv, cfg.D), g, torch.bfloat16)
+    q = _randn((B, cfg.Hq, cfg.D), g, torch.bfloat16)
+    return DecodeInputsQ8(cfg, ctx_t.to(torch.int32), ctx_t.to(torch.int32), lens.to(torch.int32), bt, kq, vq,
+                          ks.to(torch.float32), vs.to(torch.float32), k_new, v_new, q, cfg.softmax_scale)
+
+
+def decode_kv_bytes_q8(ctx_lens: torch.Tensor, Hkv: int, D: int) -> int:
+    """Algorithmic KV bytes of one INT8 decode step: codes of K and V plus
+    their two float32 row scales, for every attended token of every KV head."""
+    return int(ctx_lens.to(torch.int64).sum().item()) * Hkv * (2 * D + 8)
