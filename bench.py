@@ -210,6 +210,7 @@ class Step:
         self.merge_bytes = 3 * T * H * D * 2 + 3 * H * T * 4
         # attn x4 (+ the key-bound pass of the two D=64 calls), append, decode split + reduce, merge
         self.launches_per_step = 10
+        self.decode_ms_ref = None  # bf16 append + decode time of the step, for the INT8 comparison
 
     @property
     def step_flops(self):
@@ -350,6 +351,13 @@ def next_rows(step, K, W, pk):
     p_flops = workloads.prefill_flops(pf.start_pos, pc.T, pc.Hq, pc.D, pc.causal)
     lc = step.large.cfg
     l_lens = torch.full((lc.B,), lc.Pk - step.large.n_pad, dtype=torch.int32, device=dev)
+    dq8 = workloads.make_decode_inputs_q8(workloads.DECODE_CONFIGS["decode"], seed=0)
+    q8 = {k: getattr(dq8, k).to(dev) for k in ("kq_cache", "vq_cache", "k_scale", "v_scale", "block_table", "pos",
+                                               "ctx_lens", "k_new", "v_new", "q")}
+    q8_out = torch.empty_like(q8["q"])
+    c8 = dq8.cfg
+    q8_bytes = (workloads.decode_kv_bytes_q8(dq8.ctx_lens, c8.Hkv, c8.D) + 2 * c8.B * c8.Hq * c8.D * 2 +
+                int(((dq8.ctx_lens.to(torch.int64) + 15) // 16).sum()) * 4)
 
     def fused():
         lib.paged_decode_attn_append(step.dq, step.kn, step.vn, step.kc, step.vc, step.bt, step.pos, d.scale,
@@ -358,6 +366,12 @@ def next_rows(step, K, W, pk):
     def varlen():
         lib.attn_fwd_varlen(step.l_q, step.l_k, step.l_v, l_lens, step.large.scale, out=step.l_o, lse=step.l_l,
                             workspace=step.ws_attn)
+
+    def decode_q8():
+        lib.kv_append_q8(q8["kq_cache"], q8["vq_cache"], q8["k_scale"], q8["v_scale"], q8["block_table"], q8["pos"],
+                         q8["k_new"], q8["v_new"], workspace=step.ws_dec)
+        lib.paged_decode_attn_q8(q8["q"], q8["kq_cache"], q8["vq_cache"], q8["k_scale"], q8["v_scale"],
+                                 q8["block_table"], q8["ctx_lens"], dq8.scale, out=q8_out, workspace=step.ws_dec)
 
     def prefill():
         lib.paged_prefill_attn(p_q, p_kc, p_vc, p_bt, p_sp, k_new=p_kn, v_new=p_vn, causal=True, scale=pf.scale,
@@ -375,7 +389,7 @@ def next_rows(step, K, W, pk):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / K
 
-    f_ms, v_ms, p_ms = time_it(fused), time_it(varlen), time_it(prefill)
+    f_ms, v_ms, p_ms, q_ms = time_it(fused), time_it(varlen), time_it(prefill), time_it(decode_q8)
     peak_t = pk["bf16_tflops_sustained"]
     f_gbs = step.decode_bytes / (f_ms * 1e-3) / 1e9
     v_tf = step.flops_large / (v_ms * 1e-3) / 1e12
@@ -385,6 +399,11 @@ def next_rows(step, K, W, pk):
                                      "ms": f_ms, "gbs": f_gbs, "frac": f_gbs / pk["hbm_gbs"], "launches": 2},
         "attn_fwd_varlen": {"workload": "patch_large with key lengths (B 1, H 16, P 32000, D 64, 128 padded keys)",
                             "ms": v_ms, "tflops": v_tf, "frac": v_tf / peak_t, "launches": 1},
+        "paged_decode_attn_q8": {"workload": "decode with an INT8 cache (codes + one float32 scale per token row)",
+                                 "ms": q_ms, "gbs": q8_bytes / (q_ms * 1e-3) / 1e9,
+                                 "frac": q8_bytes / (q_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                                 "speedup_vs_bf16_decode": (step.decode_ms_ref / q_ms) if step.decode_ms_ref else None,
+                                 "launches": 3, "bytes": q8_bytes},
         "paged_prefill_attn": {"workload": "prefill_chunk (16 seqs x 1024-token causal chunk after U[0, 7168] "
                                            "cached, Hq 32, Hkv 8, D 128)",
                                "ms": p_ms, "tflops": p_tf, "frac": p_tf / peak_t, "launches": 2,
@@ -530,6 +549,7 @@ def main():
         "clocks": clk,
         "gpu_launches": step.launches_per_step * args.steps,
     }
+    step.decode_ms_ref = seg["append"] + seg["decode"]
     if not args.no_next:
         line["next"] = next_rows(step, max(5, args.steps // 2), max(3, args.warmup), pk)
     if not args.no_e2e:

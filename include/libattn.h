@@ -301,6 +301,53 @@ attn_status paged_prefill_attn(const attn_tensor *q, const attn_tensor *k_new, c
                                void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * An INT8 paged KV cache ("LLM inference memory accounting", section 18: BF16
+ * KV held as INT8 halves the payload and adds scale metadata and a
+ * dequantisation step).  K and V codes [num_blocks, num_kv_heads, block_size,
+ * head_dim] int8 (contiguous), and one float32 scale per token row of K and of
+ * V, [num_blocks, num_kv_heads, block_size] (contiguous): a row's value is
+ * code * scale.  All four pointers 16-byte aligned.
+ */
+typedef struct attn_kv_cache_q8 {
+    void *k;              /* int8 codes */
+    void *v;
+    float *k_scale;
+    float *v_scale;
+    int64_t num_blocks;
+    int32_t block_size;   /* 16 */
+    int32_t num_kv_heads;
+    int32_t head_dim;     /* 64 or 128 */
+    int32_t reserved;     /* 0 */
+} attn_kv_cache_q8;
+
+/*
+ * kv_append_q8 -- kv_append into an INT8 cache: for every sequence b (pos[b]
+ * >= 0) and KV head g, the new token's K row x = k_new[b, g, :] (and likewise
+ * V) is quantised with one scale per row, every step in float32:
+ *     a = max_d |x_d|,  scale = a / 127,  code_d = clamp(rint(x_d / scale), -127, 127)
+ * (IEEE division, rint rounding half to even; an all-zero row gets scale 0
+ * and codes 0) and written to block block_table[b][pos[b]/16], slot pos[b] % 16.
+ * Positions and block ids are checked as in kv_append.
+ *   k_new, v_new [batch, Hkv, head_dim] bf16
+ */
+attn_status kv_append_q8(const attn_kv_cache_q8 *cache, const int32_t *block_table, int64_t bt_stride,
+                         int32_t max_blocks, const int32_t *pos,
+                         const attn_tensor *k_new, const attn_tensor *v_new,
+                         void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * paged_decode_attn_q8 -- paged_decode_attn over an INT8 cache: the same
+ * definition applied to the dequantised rows (code * scale).  Reads about half
+ * the bytes of the bf16 cache: 2 * head_dim + 8 bytes per token and KV head.
+ * Arguments, workspace size and error behaviour as paged_decode_attn.
+ */
+attn_status paged_decode_attn_q8(const attn_tensor *q, const attn_kv_cache_q8 *cache,
+                                 const int32_t *block_table, int64_t bt_stride, int32_t max_blocks,
+                                 const int32_t *ctx_lens, float scale,
+                                 const attn_tensor *out, float *lse,
+                                 void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * paged_decode_attn_noalloc -- the same paged decode for callers that cannot
  * allocate device memory.  The pages have no counterpart to this call; it
  * exists for this library's users.

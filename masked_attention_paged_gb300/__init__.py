@@ -49,6 +49,12 @@ class AttnKVCache(ctypes.Structure):
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
 
 
+class AttnKVCacheQ8(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p), ("num_blocks", ctypes.c_int64), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -73,6 +79,7 @@ def load(build_if_missing: bool = False):
         P, I32, I64, SZ, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
         T = ctypes.POINTER(AttnTensor)
         C = ctypes.POINTER(AttnKVCache)
+        CQ = ctypes.POINTER(AttnKVCacheQ8)
         sig = {
             "attn_version": (I32, []),
             "attn_status_string": (ctypes.c_char_p, [I32]),
@@ -88,6 +95,8 @@ def load(build_if_missing: bool = False):
             "paged_decode_attn": (I32, [T, C, P, I64, I32, P, F, T, P, P, SZ, P]),
             "paged_decode_attn_append": (I32, [T, T, T, C, P, I64, I32, P, F, T, P, P, SZ, P]),
             "paged_prefill_attn": (I32, [T, T, T, C, P, I64, I32, P, I32, F, T, P, P, SZ, P]),
+            "kv_append_q8": (I32, [CQ, P, I64, I32, P, T, T, P, SZ, P]),
+            "paged_decode_attn_q8": (I32, [T, CQ, P, I64, I32, P, F, T, P, P, SZ, P]),
             "paged_kv_gather": (I32, [C, I32, P, I64, I32, P, I32, I64, P, P, SZ, P]),
             "paged_decode_attn_noalloc": (I32, [T, C, P, I64, I32, P, F, T, P, P, P]),
             "attn_check_device_status": (I32, [P, ctypes.POINTER(ctypes.c_uint32), P]),
@@ -108,7 +117,7 @@ def exported_symbols() -> list[str]:
             "attn_check_device_status", "attn_reset_device_status", "attn_status_string", "attn_version",
             "paged_decode_attn_noalloc", "attn_selftest_wait_timeout", "attn_fwd_varlen",
             "attn_key_padding_to_additive", "paged_decode_attn_append", "paged_prefill_attn",
-            "attn_fwd_workspace_size_for"]
+            "attn_fwd_workspace_size_for", "kv_append_q8", "paged_decode_attn_q8"]
 
 
 # --------------------------------------------------------------------------
@@ -424,6 +433,66 @@ def paged_prefill_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
                                 block_table.stride(0), block_table.shape[1], start_pos.data_ptr(), int(bool(causal)),
                                 float(scale), ctypes.byref(do), _ptr(lse), ws.ptr, ws.nbytes, _stream(stream))
     _check("paged_prefill_attn", st)
+    return (out, lse) if return_lse else out
+
+
+def _cache_q8(kq: torch.Tensor, vq: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor) -> AttnKVCacheQ8:
+    assert kq.dtype == torch.int8 and vq.dtype == torch.int8 and kq.shape == vq.shape
+    assert k_scale.dtype == torch.float32 and v_scale.dtype == torch.float32
+    assert tuple(k_scale.shape) == tuple(kq.shape[:3]) and tuple(v_scale.shape) == tuple(kq.shape[:3])
+    for t in (kq, vq, k_scale, v_scale):
+        assert t.is_contiguous()
+    c = AttnKVCacheQ8()
+    c.k, c.v, c.k_scale, c.v_scale = kq.data_ptr(), vq.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr()
+    c.num_blocks, c.num_kv_heads, c.block_size, c.head_dim = kq.shape
+    c.reserved = 0
+    return c
+
+
+def kv_append_q8(kq_cache: torch.Tensor, vq_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                 block_table: torch.Tensor, pos: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                 workspace: Optional[Workspace] = None, stream=None):
+    """Quantise each sequence's new K/V rows (bf16 [B, Hkv, D]) to INT8 codes
+    with one float32 scale per row and write them at pos[b]."""
+    lib = load()
+    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1
+    assert pos.dtype == torch.int32 and pos.is_contiguous()
+    ws = workspace or _small_ws(kq_cache.device)
+    c = _cache_q8(kq_cache, vq_cache, k_scale, v_scale)
+    dk, dv = _desc(k_new), _desc(v_new)
+    st = lib.kv_append_q8(ctypes.byref(c), block_table.data_ptr(), block_table.stride(0), block_table.shape[1],
+                          pos.data_ptr(), ctypes.byref(dk), ctypes.byref(dv), ws.ptr, ws.nbytes, _stream(stream))
+    _check("kv_append_q8", st)
+
+
+def paged_decode_attn_q8(q: torch.Tensor, kq_cache: torch.Tensor, vq_cache: torch.Tensor, k_scale: torch.Tensor,
+                         v_scale: torch.Tensor, block_table: torch.Tensor, ctx_lens: torch.Tensor,
+                         scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                         lse: Optional[torch.Tensor] = None, return_lse: bool = False,
+                         workspace: Optional[Workspace] = None, stream=None):
+    """paged_decode_attn over an INT8 cache (codes int8 [N, Hkv, 16, D],
+    scales float32 [N, Hkv, 16])."""
+    lib = load()
+    B, Hq, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1
+    assert ctx_lens.dtype == torch.int32 and ctx_lens.is_contiguous()
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    max_blocks = block_table.shape[1]
+    need = paged_decode_workspace_size(B, Hq, max_blocks, kq_cache.shape[2], D)
+    ws = workspace
+    if ws is None or ws.nbytes < need:
+        ws = Workspace(need, device=q.device)
+    c = _cache_q8(kq_cache, vq_cache, k_scale, v_scale)
+    dq, do = _desc(q), _desc(out)
+    st = lib.paged_decode_attn_q8(ctypes.byref(dq), ctypes.byref(c), block_table.data_ptr(), block_table.stride(0),
+                                  max_blocks, ctx_lens.data_ptr(), float(scale), ctypes.byref(do), _ptr(lse),
+                                  ws.ptr, ws.nbytes, _stream(stream))
+    _check("paged_decode_attn_q8", st)
     return (out, lse) if return_lse else out
 
 

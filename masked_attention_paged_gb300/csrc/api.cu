@@ -73,6 +73,31 @@ attn_status check_cache(const attn_kv_cache* c) {
   return ATTN_OK;
 }
 
+attn_status check_cache_q8(const attn_kv_cache_q8* c) {
+  if (c == nullptr || c->k == nullptr || c->v == nullptr || c->k_scale == nullptr || c->v_scale == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (c->num_blocks <= 0 || c->num_kv_heads <= 0 || c->block_size <= 0 || c->head_dim <= 0)
+    return ATTN_ERR_INVALID_ARG;
+  if (c->block_size != 16) return ATTN_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(c->k, 16) || !aligned(c->v, 16) || !aligned(c->k_scale, 16) || !aligned(c->v_scale, 16))
+    return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+PagedCache paged_q8(const attn_kv_cache_q8* c) {
+  PagedCache p;
+  p.k = c->k;
+  p.v = c->v;
+  p.k_scale = c->k_scale;
+  p.v_scale = c->v_scale;
+  p.num_blocks = c->num_blocks;
+  p.block_size = c->block_size;
+  p.Hkv = c->num_kv_heads;
+  p.D = c->head_dim;
+  return p;
+}
+
 PagedCache paged(const attn_kv_cache* c) {
   PagedCache p;
   p.k = c->k;
@@ -243,18 +268,18 @@ attn_status attn_lse_merge(int32_t n, const attn_tensor* outs, const float* cons
   return from_cuda(launch_lse_merge(a, stream));
 }
 
-attn_status kv_append(const attn_kv_cache* cache, const int32_t* block_table, int64_t bt_stride,
-                      int32_t max_blocks, const int32_t* pos, const attn_tensor* k_new, const attn_tensor* v_new,
-                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+static attn_status kv_append_core(const PagedCache& pc, const int32_t* block_table, int64_t bt_stride,
+                                  int32_t max_blocks, const int32_t* pos, const attn_tensor* k_new,
+                                  const attn_tensor* v_new, void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream) {
   attn_status st;
-  if ((st = check_cache(cache)) != ATTN_OK) return st;
   if ((st = check_tensor(k_new, 3)) != ATTN_OK) return st;
   if ((st = check_tensor(v_new, 3)) != ATTN_OK) return st;
   const int64_t B = k_new->shape[0];
   if (k_new->dtype != ATTN_BF16 || v_new->dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
   for (int i = 0; i < 3; ++i)
     if (v_new->shape[i] != k_new->shape[i]) return ATTN_ERR_INVALID_ARG;
-  if (k_new->shape[1] != cache->num_kv_heads || k_new->shape[2] != cache->head_dim) return ATTN_ERR_INVALID_ARG;
+  if (k_new->shape[1] != pc.Hkv || k_new->shape[2] != pc.D) return ATTN_ERR_INVALID_ARG;
   if ((st = check_workspace(workspace, workspace_bytes, kv_append_workspace_size())) != ATTN_OK) return st;
   if (B == 0) return ATTN_OK;
   if (B > 0x7fffffff) return ATTN_ERR_UNSUPPORTED;
@@ -262,7 +287,7 @@ attn_status kv_append(const attn_kv_cache* cache, const int32_t* block_table, in
   if (B > 1 && bt_stride < max_blocks) return ATTN_ERR_INVALID_ARG;
   if (!vec16_ok(k_new) || !vec16_ok(v_new)) return ATTN_ERR_INVALID_ARG;
   AppendArgs a;
-  a.cache = paged(cache);
+  a.cache = pc;
   a.block_table = block_table;
   a.bt_stride = bt_stride;
   a.max_blocks = max_blocks;
@@ -271,7 +296,25 @@ attn_status kv_append(const attn_kv_cache* cache, const int32_t* block_table, in
   a.k_new = view(k_new);
   a.v_new = view(v_new);
   a.status = static_cast<uint32_t*>(workspace);
-  return from_cuda(launch_kv_append(a, stream));
+  return from_cuda(pc.k_scale != nullptr ? launch_kv_append_q8(a, stream) : launch_kv_append(a, stream));
+}
+
+attn_status kv_append(const attn_kv_cache* cache, const int32_t* block_table, int64_t bt_stride,
+                      int32_t max_blocks, const int32_t* pos, const attn_tensor* k_new, const attn_tensor* v_new,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  attn_status st;
+  if ((st = check_cache(cache)) != ATTN_OK) return st;
+  return kv_append_core(paged(cache), block_table, bt_stride, max_blocks, pos, k_new, v_new, workspace,
+                        workspace_bytes, stream);
+}
+
+attn_status kv_append_q8(const attn_kv_cache_q8* cache, const int32_t* block_table, int64_t bt_stride,
+                         int32_t max_blocks, const int32_t* pos, const attn_tensor* k_new, const attn_tensor* v_new,
+                         void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  attn_status st;
+  if ((st = check_cache_q8(cache)) != ATTN_OK) return st;
+  return kv_append_core(paged_q8(cache), block_table, bt_stride, max_blocks, pos, k_new, v_new, workspace,
+                        workspace_bytes, stream);
 }
 
 attn_status paged_kv_gather(const attn_kv_cache* cache, int32_t which, const int32_t* block_table,
@@ -302,28 +345,27 @@ attn_status paged_kv_gather(const attn_kv_cache* cache, int32_t which, const int
 }
 
 static attn_status paged_decode_impl(const attn_tensor* q, const attn_tensor* k_new, const attn_tensor* v_new,
-                                     const attn_kv_cache* cache, const int32_t* block_table, int64_t bt_stride,
+                                     const PagedCache& pc, const int32_t* block_table, int64_t bt_stride,
                                      int32_t max_blocks, const int32_t* lens_or_pos, float scale,
                                      const attn_tensor* out, float* lse, void* workspace, size_t workspace_bytes,
                                      cudaStream_t stream) {
   const int32_t* ctx_lens = lens_or_pos;
   attn_status st;
-  if ((st = check_cache(cache)) != ATTN_OK) return st;
   if ((st = check_tensor(q, 3)) != ATTN_OK) return st;
   if ((st = check_tensor(out, 3)) != ATTN_OK) return st;
   const int64_t B = q->shape[0], Hq = q->shape[1], D = q->shape[2];
   for (int i = 0; i < 3; ++i)
     if (out->shape[i] != q->shape[i]) return ATTN_ERR_INVALID_ARG;
   if (q->dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
-  if (D != cache->head_dim) return ATTN_ERR_INVALID_ARG;
-  if (Hq <= 0 || Hq % cache->num_kv_heads != 0) return ATTN_ERR_INVALID_ARG;
-  const int64_t G = Hq / cache->num_kv_heads;
+  if (D != pc.D) return ATTN_ERR_INVALID_ARG;
+  if (Hq <= 0 || Hq % pc.Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  const int64_t G = Hq / pc.Hkv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return ATTN_ERR_UNSUPPORTED;
   if (!isfinite(scale)) return ATTN_ERR_INVALID_ARG;
   if (max_blocks <= 0 || max_blocks > (1 << 24)) return ATTN_ERR_INVALID_ARG;
   if (B > 65535 || B * Hq > (int64_t(1) << 30)) return ATTN_ERR_UNSUPPORTED;
   const size_t need = paged_decode_workspace_size(static_cast<int32_t>(B), static_cast<int32_t>(Hq), max_blocks,
-                                                  cache->block_size, cache->head_dim);
+                                                  pc.block_size, pc.D);
   if ((st = check_workspace(workspace, workspace_bytes, need)) != ATTN_OK) return st;
   if (B == 0) return ATTN_OK;
   if (block_table == nullptr || ctx_lens == nullptr) return ATTN_ERR_INVALID_ARG;
@@ -339,12 +381,12 @@ static attn_status paged_decode_impl(const attn_tensor* q, const attn_tensor* k_
     if (k_new->dtype != ATTN_BF16 || v_new->dtype != ATTN_BF16) return ATTN_ERR_INVALID_ARG;
     for (int i = 0; i < 3; ++i)
       if (v_new->shape[i] != k_new->shape[i]) return ATTN_ERR_INVALID_ARG;
-    if (k_new->shape[0] != B || k_new->shape[1] != cache->num_kv_heads || k_new->shape[2] != D)
+    if (k_new->shape[0] != B || k_new->shape[1] != pc.Hkv || k_new->shape[2] != D)
       return ATTN_ERR_INVALID_ARG;
     if (!vec16_ok(k_new) || !vec16_ok(v_new)) return ATTN_ERR_INVALID_ARG;
   }
   DecodeArgs a;
-  a.cache = paged(cache);
+  a.cache = pc;
   a.q = view(q);
   a.k_new = fused ? view(k_new) : View4{};
   a.v_new = fused ? view(v_new) : View4{};
@@ -358,7 +400,7 @@ static attn_status paged_decode_impl(const attn_tensor* q, const attn_tensor* k_
   a.Hq = Hq;
   a.scale = scale;
   a.partials = static_cast<uint8_t*>(workspace) + kStatusBytes;
-  a.n_split = decode_num_splits(max_blocks, cache->block_size);
+  a.n_split = decode_num_splits(max_blocks, pc.block_size);
   a.status = static_cast<uint32_t*>(workspace);
   return from_cuda(launch_paged_decode(a, stream));
 }
@@ -367,8 +409,20 @@ attn_status paged_decode_attn(const attn_tensor* q, const attn_kv_cache* cache, 
                               int64_t bt_stride, int32_t max_blocks, const int32_t* ctx_lens, float scale,
                               const attn_tensor* out, float* lse, void* workspace, size_t workspace_bytes,
                               cudaStream_t stream) {
-  return paged_decode_impl(q, nullptr, nullptr, cache, block_table, bt_stride, max_blocks, ctx_lens, scale, out,
-                           lse, workspace, workspace_bytes, stream);
+  attn_status st;
+  if ((st = check_cache(cache)) != ATTN_OK) return st;
+  return paged_decode_impl(q, nullptr, nullptr, paged(cache), block_table, bt_stride, max_blocks, ctx_lens, scale,
+                           out, lse, workspace, workspace_bytes, stream);
+}
+
+attn_status paged_decode_attn_q8(const attn_tensor* q, const attn_kv_cache_q8* cache, const int32_t* block_table,
+                                 int64_t bt_stride, int32_t max_blocks, const int32_t* ctx_lens, float scale,
+                                 const attn_tensor* out, float* lse, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream) {
+  attn_status st;
+  if ((st = check_cache_q8(cache)) != ATTN_OK) return st;
+  return paged_decode_impl(q, nullptr, nullptr, paged_q8(cache), block_table, bt_stride, max_blocks, ctx_lens, scale,
+                           out, lse, workspace, workspace_bytes, stream);
 }
 
 attn_status paged_decode_attn_append(const attn_tensor* q, const attn_tensor* k_new, const attn_tensor* v_new,
@@ -376,7 +430,9 @@ attn_status paged_decode_attn_append(const attn_tensor* q, const attn_tensor* k_
                                      int32_t max_blocks, const int32_t* pos, float scale, const attn_tensor* out,
                                      float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (k_new == nullptr || v_new == nullptr) return ATTN_ERR_INVALID_ARG;
-  return paged_decode_impl(q, k_new, v_new, cache, block_table, bt_stride, max_blocks, pos, scale, out, lse,
+  attn_status st;
+  if ((st = check_cache(cache)) != ATTN_OK) return st;
+  return paged_decode_impl(q, k_new, v_new, paged(cache), block_table, bt_stride, max_blocks, pos, scale, out, lse,
                            workspace, workspace_bytes, stream);
 }
 

@@ -22,6 +22,10 @@
 // and the token itself is handed in.  Only the CTA whose split ends at that
 // position reads its slot, so it substitutes the new K/V row into its copy of
 // the block once the block has landed, and writes the row to the cache.
+// INT8 cache ("LLM inference memory accounting", section 18): the block's
+// codes (half the bytes) and its 16 per-token float32 scales of K and of V
+// are streamed together; a score is the dot product with the codes times the
+// key's scale, and a value row's scale is folded into its softmax weight.
 #include <math.h>
 
 #include "common.cuh"
@@ -48,8 +52,10 @@ constexpr int kStages = 2;                          // per-warp buffer depth
 constexpr float kLazyRescale = 8.0f;                // log2 units of headroom before a rescale
 
 struct DecodeParams {
-  const uint16_t* kc;
-  const uint16_t* vc;
+  const void* kc;  // bf16 or int8 codes
+  const void* vc;
+  const float* ks;  // INT8 cache: float32 scale per token row [num_blocks, Hkv, 16]
+  const float* vs;
   int64_t num_blocks;
   int Hkv;
   const uint16_t* q;
@@ -70,7 +76,7 @@ struct DecodeParams {
   uint32_t* status;
 };
 
-template <int D, int G>
+template <int D, int G, bool Q8>
 struct Geo {
   static constexpr int CPR = D / 8;             // 16-byte chunks per token row = lanes per token set
   static constexpr int TS = 32 / CPR;           // token sets per warp
@@ -79,15 +85,39 @@ struct Geo {
   static constexpr int R = N >= CPR ? N / CPR : 1;  // scores a lane keeps after the reduce
   static constexpr int SHARE = N >= CPR ? 1 : CPR / N;  // lanes holding the same score
   static constexpr int HEAD_LANES = CPR / G;    // lanes of one token set holding one head
-  static constexpr int BLOCK_BYTES = kBS * D * 2;
+  static constexpr int EB = Q8 ? 1 : 2;         // bytes per element
+  static constexpr int BLOCK_BYTES = kBS * D * EB;
+  static constexpr int SCALE_BYTES = Q8 ? kBS * 4 : 0;  // one block's row scales, K or V
+  static constexpr int STAGE_BYTES = 2 * BLOCK_BYTES + 2 * SCALE_BYTES;
 };
 
-template <int D, int G>
+// 8 consecutive elements of a row as floats: 8 bf16 (16 bytes) or 8 int8 codes (8 bytes)
+template <bool Q8>
+__device__ __forceinline__ void load8(const uint8_t* src, float f[8]) {
+  if constexpr (Q8) {
+    // code b -> the float 2^23 + (b + 128) (its byte placed in a mantissa
+    // whose unit is 1), minus 2^23 + 128: exact, and on the full-rate integer
+    // and FMA pipes rather than the conversion unit
+    const uint2 w = *reinterpret_cast<const uint2*>(src);
+    const uint32_t x0 = w.x ^ 0x80808080u, x1 = w.y ^ 0x80808080u;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      f[e] = __uint_as_float(__byte_perm(x0, 0x4B000000u, 0x7540u | e)) - 8388736.0f;
+      f[4 + e] = __uint_as_float(__byte_perm(x1, 0x4B000000u, 0x7540u | e)) - 8388736.0f;
+    }
+  } else {
+    const uint4 w = *reinterpret_cast<const uint4*>(src);
+    f[0] = bf16lo_to_f32(w.x); f[1] = bf16hi_to_f32(w.x); f[2] = bf16lo_to_f32(w.y); f[3] = bf16hi_to_f32(w.y);
+    f[4] = bf16lo_to_f32(w.z); f[5] = bf16hi_to_f32(w.z); f[6] = bf16lo_to_f32(w.w); f[7] = bf16hi_to_f32(w.w);
+  }
+}
+
+template <int D, int G, bool Q8>
 __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeParams p) {
-  using Gm = Geo<D, G>;
+  using Gm = Geo<D, G, Q8>;
   extern __shared__ __align__(128) uint8_t smem[];
-  // per warp: kStages x {K block, V block}
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * 2 * Gm::BLOCK_BYTES);
+  // per warp: kStages x {K block, V block[, K scales, V scales]}
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kWarps * kStages * Gm::STAGE_BYTES);
   float* comb = reinterpret_cast<float*>(bars + kWarps * kStages);  // [kWarps][G][D + 2]
 
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
@@ -108,12 +138,12 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeP
   // fused append: the new token is the last of the context (when it fits the
   // table); i_new is this warp's iteration over its block, or -1
   int i_new = -1;
-  if (p.k_new != nullptr && L_req >= 1 && L_req == L && L - 1 >= t_begin) {
+  if (!Q8 && p.k_new != nullptr && L_req >= 1 && L_req == L && L - 1 >= t_begin) {
     const int rel = (L - 1) / kBS - lb0;
     if (rel % kWarps == warp) i_new = rel / kWarps;
   }
 
-  uint8_t* wbuf = smem + warp * kStages * 2 * Gm::BLOCK_BYTES;
+  uint8_t* wbuf = smem + warp * kStages * Gm::STAGE_BYTES;
   uint64_t* wbar = bars + warp * kStages;
   if (lane == 0)
     for (int s = 0; s < kStages; ++s) mbar_init(&wbar[s], 1);
@@ -137,12 +167,17 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeP
       mbar_arrive(&wbar[s]);
       return;
     }
-    uint8_t* dst = wbuf + s * 2 * Gm::BLOCK_BYTES;
-    const int64_t off = (static_cast<int64_t>(blk) * p.Hkv + g) * (kBS * D);
+    uint8_t* dst = wbuf + s * Gm::STAGE_BYTES;
+    const int64_t row = static_cast<int64_t>(blk) * p.Hkv + g;  // (block, KV head) slab
     fence_proxy_async_smem();
-    mbar_arrive_expect_tx(&wbar[s], 2 * Gm::BLOCK_BYTES);
-    bulk_load(dst, p.kc + off, Gm::BLOCK_BYTES, &wbar[s]);
-    bulk_load(dst + Gm::BLOCK_BYTES, p.vc + off, Gm::BLOCK_BYTES, &wbar[s]);
+    mbar_arrive_expect_tx(&wbar[s], Gm::STAGE_BYTES);
+    bulk_load(dst, static_cast<const uint8_t*>(p.kc) + row * Gm::BLOCK_BYTES, Gm::BLOCK_BYTES, &wbar[s]);
+    bulk_load(dst + Gm::BLOCK_BYTES, static_cast<const uint8_t*>(p.vc) + row * Gm::BLOCK_BYTES, Gm::BLOCK_BYTES,
+              &wbar[s]);
+    if constexpr (Q8) {
+      bulk_load(dst + 2 * Gm::BLOCK_BYTES, p.ks + row * kBS, Gm::SCALE_BYTES, &wbar[s]);
+      bulk_load(dst + 2 * Gm::BLOCK_BYTES + Gm::SCALE_BYTES, p.vs + row * kBS, Gm::SCALE_BYTES, &wbar[s]);
+    }
   };
 
   // q of this lane's 8 dims for every head of the group, pre-scaled to log2 units
@@ -158,6 +193,13 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeP
       qf[hh][2 * e + 1] = bf16hi_to_f32(wv[e]) * p.scale_log2;
     }
   }
+  // q as packed pairs: every dot product and output update below takes two
+  // fp32 lanes per fma.rn.f32x2
+  uint64_t q2[G][4];
+#pragma unroll
+  for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) q2[hh][e] = f2_pack(qf[hh][2 * e], qf[hh][2 * e + 1]);
   float o[G][8];
   float m_run[G];
 #pragma unroll
@@ -194,8 +236,10 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeP
       break;
     }
     if (blk >= 0) {
-      uint8_t* kb = wbuf + s * 2 * Gm::BLOCK_BYTES;
+      uint8_t* kb = wbuf + s * Gm::STAGE_BYTES;
       uint8_t* vb = kb + Gm::BLOCK_BYTES;
+      const float* ksb = reinterpret_cast<const float*>(kb + 2 * Gm::BLOCK_BYTES);  // Q8 only
+      const float* vsb = ksb + kBS;
       if (i == i_new) {
         // the block has landed: put the new token's row in place of whatever
         // the slot held, and store it to the cache (lanes [0, CPR) carry K's
@@ -208,7 +252,7 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeP
                                      : p.k_new + b * p.kn_stride[0] + g * p.kn_stride[1];
           const uint4 w = *reinterpret_cast<const uint4*>(src + c * 8);
           *reinterpret_cast<uint4*>((is_v ? vb : kb) + slot * (D * 2) + c * 16) = w;
-          uint16_t* cache = const_cast<uint16_t*>(is_v ? p.vc : p.kc);
+          uint16_t* cache = static_cast<uint16_t*>(const_cast<void*>(is_v ? p.vc : p.kc));
           const int64_t off = (static_cast<int64_t>(blk) * p.Hkv + g) * (kBS * D) + slot * D + c * 8;
           *reinterpret_cast<uint4*>(cache + off) = w;
         }
@@ -221,15 +265,18 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeP
 #pragma unroll
       for (int i2 = 0; i2 < Gm::TPL; ++i2) {
         const int t = Gm::TS * i2 + ts;
-        const uint4 kw = *reinterpret_cast<const uint4*>(kb + t * (D * 2) + cl * 16);
-        const float kf[8] = {bf16lo_to_f32(kw.x), bf16hi_to_f32(kw.x), bf16lo_to_f32(kw.y), bf16hi_to_f32(kw.y),
-                             bf16lo_to_f32(kw.z), bf16hi_to_f32(kw.z), bf16lo_to_f32(kw.w), bf16hi_to_f32(kw.w)};
+        float kf[8];
+        load8<Q8>(kb + t * (D * Gm::EB) + cl * 8 * Gm::EB, kf);
+        const uint64_t k2[4] = {f2_pack(kf[0], kf[1]), f2_pack(kf[2], kf[3]), f2_pack(kf[4], kf[5]),
+                                f2_pack(kf[6], kf[7])};
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
-          float a = qf[hh][0] * kf[0];
+          uint64_t a2 = ffma2(q2[hh][0], k2[0], 0ull);
 #pragma unroll
-          for (int e = 1; e < 8; ++e) a = fmaf(qf[hh][e], kf[e], a);
-          acc[hh * Gm::TPL + i2] = a;
+          for (int e = 1; e < 4; ++e) a2 = ffma2(q2[hh][e], k2[e], a2);
+          float lo, hi;
+          f2_unpack(a2, lo, hi);
+          acc[hh * Gm::TPL + i2] = lo + hi;
         }
       }
       // transposing reduce over the CPR lanes of a token set: each stage
@@ -258,7 +305,8 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeP
       for (int k = 0; k < Gm::R; ++k) {
         const int idx = my_idx0 + k;
         const int t = Gm::TS * (idx % Gm::TPL) + ts;
-        sc[k] = (tok0 + t < t_end) ? acc[k] : -INFINITY;
+        // INT8: the dot product with the codes times the key row's scale
+        sc[k] = (tok0 + t < t_end) ? (Q8 ? acc[k] * ksb[t] : acc[k]) : -INFINITY;
         mx = fmaxf(mx, sc[k]);
       }
       // block max of each head: lanes of the head within the token set, then across token sets
@@ -302,13 +350,17 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeP
       for (int i2 = 0; i2 < Gm::TPL; ++i2) {
         const int t = Gm::TS * i2 + ts;
         if (tok0 + t >= t_end) continue;  // slots past the context may hold anything (even NaN)
-        const uint4 vw = *reinterpret_cast<const uint4*>(vb + t * (D * 2) + cl * 16);
-        const float vf[8] = {bf16lo_to_f32(vw.x), bf16hi_to_f32(vw.x), bf16lo_to_f32(vw.y), bf16hi_to_f32(vw.y),
-                             bf16lo_to_f32(vw.z), bf16hi_to_f32(vw.z), bf16lo_to_f32(vw.w), bf16hi_to_f32(vw.w)};
+        float vf[8];
+        load8<Q8>(vb + t * (D * Gm::EB) + cl * 8 * Gm::EB, vf);
+        const float vsc = Q8 ? vsb[t] : 1.0f;  // INT8: the value row's scale joins its weight
+        const uint64_t v2[4] = {f2_pack(vf[0], vf[1]), f2_pack(vf[2], vf[3]), f2_pack(vf[4], vf[5]),
+                                f2_pack(vf[6], vf[7])};
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
+          const float w = Q8 ? pv[hh][i2] * vsc : pv[hh][i2];
+          const uint64_t w2 = f2_pack(w, w);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[hh][e] = fmaf(pv[hh][i2], vf[e], o[hh][e]);
+          for (int e = 0; e < 4; ++e) f2_unpack(ffma2(w2, v2[e], f2_pack(o[hh][2 * e], o[hh][2 * e + 1])), o[hh][2 * e], o[hh][2 * e + 1]);
         }
       }
     }
@@ -430,11 +482,11 @@ __global__ void decode_reduce_kernel(const float* __restrict__ o_part, const flo
     lse[wid] = empty ? -INFINITY : (M + __log2f(wsum)) * 0.6931471805599453f;
 }
 
-template <int D, int G>
+template <int D, int G, bool Q8>
 cudaError_t launch_decode(const DecodeArgs& a, const DecodeParams& p, cudaStream_t stream) {
-  using Gm = Geo<D, G>;
-  const int smem = kWarps * kStages * 2 * Gm::BLOCK_BYTES + kWarps * kStages * 8 + kWarps * G * (D + 2) * 4;
-  auto kern = paged_decode_kernel<D, G>;
+  using Gm = Geo<D, G, Q8>;
+  const int smem = kWarps * kStages * Gm::STAGE_BYTES + kWarps * kStages * 8 + kWarps * G * (D + 2) * 4;
+  auto kern = paged_decode_kernel<D, G, Q8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(a.n_split), static_cast<unsigned>(a.cache.Hkv), static_cast<unsigned>(a.B));
@@ -450,13 +502,13 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodeParams& p, cudaStream
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool Q8>
 cudaError_t launch_decode_d(const DecodeArgs& a, const DecodeParams& p, cudaStream_t stream) {
   switch (a.Hq / a.cache.Hkv) {
-    case 1: return launch_decode<D, 1>(a, p, stream);
-    case 2: return launch_decode<D, 2>(a, p, stream);
-    case 4: return launch_decode<D, 4>(a, p, stream);
-    case 8: return launch_decode<D, 8>(a, p, stream);
+    case 1: return launch_decode<D, 1, Q8>(a, p, stream);
+    case 2: return launch_decode<D, 2, Q8>(a, p, stream);
+    case 4: return launch_decode<D, 4, Q8>(a, p, stream);
+    case 8: return launch_decode<D, 8, Q8>(a, p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -465,8 +517,10 @@ cudaError_t launch_decode_d(const DecodeArgs& a, const DecodeParams& p, cudaStre
 
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
   DecodeParams p;
-  p.kc = static_cast<const uint16_t*>(a.cache.k);
-  p.vc = static_cast<const uint16_t*>(a.cache.v);
+  p.kc = a.cache.k;
+  p.vc = a.cache.v;
+  p.ks = a.cache.k_scale;
+  p.vs = a.cache.v_scale;
   p.num_blocks = a.cache.num_blocks;
   p.Hkv = a.cache.Hkv;
   p.q = static_cast<const uint16_t*>(a.q.data);
@@ -490,8 +544,10 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.n_split = a.n_split;
   p.Hq = static_cast<int>(a.Hq);
   p.status = a.status;
-  if (a.cache.D == 64) return launch_decode_d<64>(a, p, stream);
-  if (a.cache.D == 128) return launch_decode_d<128>(a, p, stream);
+  const bool q8 = a.cache.k_scale != nullptr;
+  if (a.cache.D == 64) return q8 ? launch_decode_d<64, true>(a, p, stream) : launch_decode_d<64, false>(a, p, stream);
+  if (a.cache.D == 128)
+    return q8 ? launch_decode_d<128, true>(a, p, stream) : launch_decode_d<128, false>(a, p, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -49,8 +49,10 @@ struct MergeArgs {
 cudaError_t launch_lse_merge(const MergeArgs& a, cudaStream_t stream);
 
 struct PagedCache {
-  void* k;
+  void* k;  // bf16, or int8 codes when k_scale is set
   void* v;
+  const float* k_scale = nullptr;  // INT8 cache: float32 per token row [num_blocks, Hkv, block_size]
+  const float* v_scale = nullptr;
   int64_t num_blocks;
   int block_size;
   int Hkv;
@@ -68,6 +70,8 @@ struct AppendArgs {
   uint32_t* status;
 };
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
+// INT8 cache (a.cache.k_scale set): quantise and write the new token's rows
+cudaError_t launch_kv_append_q8(const AppendArgs& a, cudaStream_t stream);
 
 struct GatherArgs {
   PagedCache cache;

@@ -62,6 +62,82 @@ __global__ void kv_append_kernel(const AppendParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// kv_append_q8: quantise one new token's K and V rows per KV head (one warp per
+// row pair) and write codes and scales.  Every step in float32 as the INT8
+// definition reads: a = max |x|, scale = a / 127, code = clamp(rint(x / scale),
+// -127, 127) with IEEE division and round-half-even (0 / 0 for a zero row).
+// ---------------------------------------------------------------------------
+struct AppendQ8Params {
+  int8_t* kq;
+  int8_t* vq;
+  float* ks;
+  float* vs;
+  int64_t num_blocks;
+  int Hkv, D;
+  const int32_t* bt;
+  int64_t bt_stride;
+  int max_blocks;
+  const int32_t* pos;
+  const uint16_t* kn;
+  const uint16_t* vn;
+  int64_t kn_stride[2], vn_stride[2];  // batch, head (elements)
+  uint32_t* status;
+};
+
+template <int D>
+__device__ __forceinline__ void quantise_row_q8(const uint16_t* src, int8_t* dst, float* scale_out, int lane) {
+  constexpr int E = D / 32;  // elements per lane
+  float x[E];
+  float a = 0.0f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    x[e] = __uint_as_float(static_cast<uint32_t>(src[lane * E + e]) << 16);
+    a = fmaxf(a, fabsf(x[e]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  const float scale = __fdiv_rn(a, 127.0f);
+  uint32_t packed = 0u;
+#pragma unroll
+  for (int e = 0; e < E; ++e) {
+    float c = scale > 0.0f ? rintf(__fdiv_rn(x[e], scale)) : 0.0f;
+    c = fminf(fmaxf(c, -127.0f), 127.0f);
+    packed |= (static_cast<uint32_t>(static_cast<int32_t>(c)) & 0xffu) << (8 * e);
+  }
+  if constexpr (E == 4) {
+    *reinterpret_cast<uint32_t*>(dst + lane * 4) = packed;
+  } else {
+    *reinterpret_cast<uint16_t*>(dst + lane * 2) = static_cast<uint16_t>(packed);
+  }
+  if (lane == 0) *scale_out = scale;
+}
+
+template <int D>
+__global__ void kv_append_q8_kernel(const AppendQ8Params p) {
+  constexpr int kBS = 16;
+  const int b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pos = p.pos[b];
+  if (pos < 0) return;  // idle sequence
+  const int lb = pos / kBS;
+  if (lb >= p.max_blocks) {
+    if (threadIdx.x == 0) report(p.status, kStatusBounds);
+    return;
+  }
+  const int blk = p.bt[static_cast<int64_t>(b) * p.bt_stride + lb];
+  if (blk < 0 || blk >= p.num_blocks) {
+    if (threadIdx.x == 0) report(p.status, kStatusBounds);
+    return;
+  }
+  const int slot = pos % kBS;
+  for (int g = warp; g < p.Hkv; g += blockDim.x >> 5) {
+    const int64_t row = (static_cast<int64_t>(blk) * p.Hkv + g) * kBS + slot;
+    quantise_row_q8<D>(p.kn + b * p.kn_stride[0] + g * p.kn_stride[1], p.kq + row * D, p.ks + row, lane);
+    quantise_row_q8<D>(p.vn + b * p.vn_stride[0] + g * p.vn_stride[1], p.vq + row * D, p.vs + row, lane);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // kv_append_chunk: token i of sequence b's chunk (k_new[b, g, i, :]) goes to
 // position start_pos[b] + i.  grid (vector tiles, B); 16-byte vectors, the
 // dim chunk fastest, then the token, then the head, so consecutive threads
@@ -289,6 +365,37 @@ cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
   p.status = a.status;
   const int threads = std::min(256, std::max(32, a.cache.Hkv * a.cache.D / 8));
   kv_append_kernel<<<static_cast<unsigned>(a.B), threads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_append_q8(const AppendArgs& a, cudaStream_t stream) {
+  AppendQ8Params p;
+  p.kq = static_cast<int8_t*>(a.cache.k);
+  p.vq = static_cast<int8_t*>(a.cache.v);
+  p.ks = const_cast<float*>(a.cache.k_scale);
+  p.vs = const_cast<float*>(a.cache.v_scale);
+  p.num_blocks = a.cache.num_blocks;
+  p.Hkv = a.cache.Hkv;
+  p.D = a.cache.D;
+  p.bt = a.block_table;
+  p.bt_stride = a.bt_stride;
+  p.max_blocks = a.max_blocks;
+  p.pos = a.pos;
+  p.kn = static_cast<const uint16_t*>(a.k_new.data);
+  p.vn = static_cast<const uint16_t*>(a.v_new.data);
+  p.kn_stride[0] = a.k_new.stride[0];
+  p.kn_stride[1] = a.k_new.stride[1];
+  p.vn_stride[0] = a.v_new.stride[0];
+  p.vn_stride[1] = a.v_new.stride[1];
+  p.status = a.status;
+  const int threads = std::min(256, std::max(32, a.cache.Hkv * 32));
+  if (a.cache.D == 128) {
+    kv_append_q8_kernel<128><<<static_cast<unsigned>(a.B), threads, 0, stream>>>(p);
+  } else if (a.cache.D == 64) {
+    kv_append_q8_kernel<64><<<static_cast<unsigned>(a.B), threads, 0, stream>>>(p);
+  } else {
+    return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 

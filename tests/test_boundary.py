@@ -276,3 +276,32 @@ def test_paged_prefill_rejects(L):
     assert call(scale=float("nan")) == INVALID
     assert call(bts=5) == INVALID
     assert call(q=_t([2, 8, 0, 128]), out=_t([2, 8, 0, 128])) == OK  # empty chunk: nothing launched
+
+
+def _cache_q8(D=128, nb=100, H=8, bs=16, k=FAKE, ks=FAKE):
+    c = lib.AttnKVCacheQ8()
+    c.k, c.v, c.k_scale, c.v_scale = k, FAKE, ks, FAKE
+    c.num_blocks, c.block_size, c.num_kv_heads, c.head_dim, c.reserved = nb, bs, H, D, 0
+    return c
+
+
+def test_q8_calls_reject(L):
+    kn = _t([4, 8, 128])
+    def app(c=None, k=kn):
+        c = c or _cache_q8()
+        return L.kv_append_q8(ctypes.byref(c), FAKE, 10, 10, FAKE, ctypes.byref(k), ctypes.byref(kn), FAKE, 256, None)
+    assert app(c=_cache_q8(ks=None)) == INVALID
+    assert app(c=_cache_q8(ks=FAKE + 4)) == INVALID  # scales must be 16-byte aligned
+    assert app(c=_cache_q8(bs=32)) == UNSUPPORTED
+    assert app(c=_cache_q8(D=96)) == UNSUPPORTED
+    assert app(k=_t([4, 8, 64])) == INVALID  # head dim differs from the cache
+    need = L.paged_decode_workspace_size(4, 32, 10, 16, 128)
+    def dec(c=None, ws_bytes=need, q=None):
+        c = c or _cache_q8()
+        q = q or _t([4, 32, 128])
+        out = _t([4, 32, 128])
+        return L.paged_decode_attn_q8(ctypes.byref(q), ctypes.byref(c), FAKE, 10, 10, FAKE, 0.1, ctypes.byref(out),
+                                      None, FAKE, ws_bytes, None)
+    assert dec(c=_cache_q8(k=None)) == INVALID
+    assert dec(ws_bytes=need - 256) == WORKSPACE
+    assert dec(q=_t([4, 32, 128], 0)) == UNSUPPORTED  # f32 queries

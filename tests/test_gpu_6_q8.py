@@ -1,0 +1,108 @@
+"""GPU parity of the INT8 KV cache calls (memory accounting page, section 18):
+kv_append_q8's codes and scales bit for bit against the oracle's quantiser,
+and paged_decode_attn_q8 against the oracle's decode over the dequantised
+cache within the bf16 tolerances, at small ragged sizes and at the full
+decode workload.  Unfilled slots hold a NaN scale, so reading one shows."""
+import numpy as np
+import pytest
+import torch
+
+import masked_attention_paged_gb300 as lib
+import oracle
+import workloads
+from _parity import assert_lse_close, assert_out_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _dev(d):
+    return {k: getattr(d, k).to(DEV) for k in ("kq_cache", "vq_cache", "k_scale", "v_scale", "block_table", "pos",
+                                               "ctx_lens", "ctx", "k_new", "v_new", "q")}
+
+
+def _append_decode_check(d, note=""):
+    g = _dev(d)
+    ws = lib.Workspace(lib.paged_decode_workspace_size(d.cfg.B, d.cfg.Hq, d.block_table.shape[1], 16, d.cfg.D))
+    lib.kv_append_q8(g["kq_cache"], g["vq_cache"], g["k_scale"], g["v_scale"], g["block_table"], g["pos"],
+                     g["k_new"], g["v_new"], workspace=ws)
+    out, lse = lib.paged_decode_attn_q8(g["q"], g["kq_cache"], g["vq_cache"], g["k_scale"], g["v_scale"],
+                                        g["block_table"], g["ctx_lens"], d.scale, return_lse=True, workspace=ws)
+    assert ws.status() == 0
+    kq, vq, ks, vs = oracle.kv_append_q8(d.kq_cache, d.vq_cache, d.k_scale, d.v_scale, d.block_table, d.pos,
+                                         d.k_new, d.v_new)
+    np.testing.assert_array_equal(g["kq_cache"].cpu().numpy(), kq)
+    np.testing.assert_array_equal(g["vq_cache"].cpu().numpy(), vq)
+    # scales as bits (NaN sentinels included)
+    np.testing.assert_array_equal(g["k_scale"].cpu().numpy().view(np.int32), ks.view(np.int32))
+    np.testing.assert_array_equal(g["v_scale"].cpu().numpy().view(np.int32), vs.view(np.int32))
+    ro, rl = oracle.paged_decode_q8(d.q, kq, vq, ks, vs, d.block_table, d.ctx_lens, d.scale)
+    assert_out_close(out, ro, what="q8 decode out" + note)
+    assert_lse_close(lse, rl, what="q8 decode lse" + note)
+
+
+@pytest.mark.parametrize("D,G", [(128, 4), (128, 1), (128, 8), (64, 4), (64, 2)])
+def test_q8_append_and_decode_small(D, G):
+    Hkv = 2
+    cfg = workloads.DecodeConfig("q", 9, G * Hkv, Hkv, D, 16, 0, 1500, 4)
+    d = workloads.make_decode_inputs_q8(cfg, seed=51, ctx=[0, 15, 16, 511, 512, 1023, 1024, 1300, 1500])
+    _append_decode_check(d, f" D={D} G={G}")
+
+
+def test_q8_full_decode_workload():
+    d = workloads.make_decode_inputs_q8(workloads.DECODE_CONFIGS["decode"], seed=0)
+    _append_decode_check(d, " full")
+
+
+def test_q8_append_zero_rows_idle_and_bad_positions():
+    cfg = workloads.DecodeConfig("q", 4, 8, 2, 128, 16, 0, 100, 2)
+    d = workloads.make_decode_inputs_q8(cfg, seed=52, ctx=[3, 30, 60, 90])
+    d.k_new[0] = 0  # all-zero rows: scale 0, codes 0
+    g = _dev(d)
+    pos = g["pos"].clone()
+    pos[1] = -1  # idle
+    pos[2] = 16 * d.block_table.shape[1]  # past the table
+    ws = lib.Workspace(256)
+    lib.kv_append_q8(g["kq_cache"], g["vq_cache"], g["k_scale"], g["v_scale"], g["block_table"], pos,
+                     g["k_new"], g["v_new"], workspace=ws)
+    assert ws.status() == 5
+    p2 = d.pos.clone()
+    p2[1] = -1
+    p2[2] = -1
+    kq, vq, ks, vs = oracle.kv_append_q8(d.kq_cache, d.vq_cache, d.k_scale, d.v_scale, d.block_table, p2,
+                                         d.k_new, d.v_new)
+    np.testing.assert_array_equal(g["kq_cache"].cpu().numpy(), kq)
+    np.testing.assert_array_equal(g["k_scale"].cpu().numpy().view(np.int32), ks.view(np.int32))
+    blk, slot = int(d.block_table[0, int(d.pos[0]) // 16]), int(d.pos[0]) % 16
+    assert np.all(ks[blk, :, slot] == 0) and not kq[blk, :, slot].any()
+
+
+def test_q8_decode_tracks_the_bf16_decode():
+    """Quantising a bf16 cache with the library and decoding it stays close to
+    decoding the bf16 cache: the INT8 codes keep about 7 bits per element."""
+    cfg = workloads.DecodeConfig("r", 8, 32, 8, 128, 16, 200, 500, 4)
+    d = workloads.make_decode_inputs(cfg, seed=53)
+    g = {k: getattr(d, k).to(DEV) for k in ("k_cache", "v_cache", "block_table", "pos", "ctx_lens", "k_new",
+                                           "v_new", "q")}
+    lib.kv_append(g["k_cache"], g["v_cache"], g["block_table"], g["pos"], g["k_new"], g["v_new"])
+    ref = lib.paged_decode_attn(g["q"], g["k_cache"], g["v_cache"], g["block_table"], g["ctx_lens"], d.scale)
+    # the whole bf16 cache quantised row by row through kv_append_q8, one slot at a time per sequence
+    nb, H, bs, D = d.k_cache.shape
+    kq = torch.zeros(nb, H, bs, D, dtype=torch.int8, device=DEV)
+    vq = torch.zeros_like(kq)
+    ks = torch.full((nb, H, bs), float("nan"), device=DEV)
+    vs = torch.full_like(ks, float("nan"))
+    for t in range(int(d.ctx_lens.max())):
+        pos = torch.where(d.ctx_lens > t, torch.full_like(d.ctx_lens, t), torch.full_like(d.ctx_lens, -1))
+        bt = d.block_table.clone()
+        kn = torch.zeros(cfg.B, H, D, dtype=torch.bfloat16)
+        vn = torch.zeros_like(kn)
+        for b in range(cfg.B):
+            if t < int(d.ctx_lens[b]):
+                blk = int(bt[b, t // 16])
+                kn[b] = g["k_cache"][blk, :, t % 16].cpu()
+                vn[b] = g["v_cache"][blk, :, t % 16].cpu()
+        lib.kv_append_q8(kq, vq, ks, vs, g["block_table"], pos.to(DEV).to(torch.int32), kn.to(DEV), vn.to(DEV))
+    out = lib.paged_decode_attn_q8(g["q"], kq, vq, ks, vs, g["block_table"], g["ctx_lens"], d.scale)
+    err = (out.float() - ref.float()).abs()
+    assert err.max().item() < 3e-2 and err.mean().item() < 3e-3
