@@ -79,14 +79,17 @@ typedef struct attn_kv_cache {
 /* Bytes of workspace each call needs (always a multiple of 256).  The first
  * 256 bytes hold the device status word. */
 size_t attn_fwd_workspace_size(void);
-/* Workspace that lets attn_fwd take its fastest path for this shape: the
- * status word and, for head_dim 64 (bf16), the largest |k| element of every
- * 128-key tile, one float per (batch, KV head, tile), which bounds every score
- * of the tile by |q|_1 max|k| and so lets the kernel skip its softmax max pass
- * wherever that bound rules out overflow.  attn_fwd / attn_fwd_varlen accept
- * any workspace of at least attn_fwd_workspace_size() bytes and use the bounds
- * when the workspace is this large and the call is big enough for the extra
- * pass over K to pay (B * Hq * Pq * Pk * D >= 2^36).  0 for a negative size. */
+/* Workspace that lets attn_fwd take its fastest path for this shape on the
+ * current device (head_dim 64 or 128, bf16): the status word; for head_dim 64
+ * the largest |k| element of every 128-key tile, one float per (batch, KV
+ * head, tile), which bounds every score of the tile by |q|_1 max|k| and so lets
+ * the kernel skip its softmax max pass wherever that bound rules out overflow
+ * (used when B * Hq * Pq * Pk * D >= 2^36, where the extra pass over K pays);
+ * and room for the partial results of query tiles whose key tiles are split
+ * over several CTAs so that the last wave of CTAs fills the GPU (one SM's
+ * worth of 256-row partials per SM, merged by the LSE rule).  attn_fwd /
+ * attn_fwd_varlen accept any workspace of at least attn_fwd_workspace_size()
+ * bytes and use what fits.  0 for a negative size. */
 size_t attn_fwd_workspace_size_for(int32_t batch, int32_t kv_heads, int64_t num_keys, int32_t head_dim);
 size_t kv_append_workspace_size(void);
 size_t paged_decode_workspace_size(int32_t batch, int32_t num_q_heads,

@@ -133,12 +133,19 @@ const char* attn_status_string(attn_status s) {
 
 size_t attn_fwd_workspace_size(void) { return kStatusBytes; }
 
-size_t attn_fwd_workspace_size_for(int32_t batch, int32_t kv_heads, int64_t num_keys, int32_t head_dim) {
-  if (batch < 0 || kv_heads < 0 || num_keys < 0 || head_dim <= 0) return 0;
-  if (head_dim != 64) return kStatusBytes;  // the key-tile bounds serve the D = 64 kernel only
+// attn_fwd workspace: [status word][key-tile bounds (D = 64)][split-unit partials]
+static size_t key_bound_bytes(int32_t batch, int32_t kv_heads, int64_t num_keys, int32_t head_dim) {
+  if (head_dim != 64) return 0;  // the key-tile bounds serve the D = 64 kernel only
   const size_t tiles = static_cast<size_t>((num_keys + kKeyTile - 1) / kKeyTile);
   const size_t bytes = static_cast<size_t>(batch) * kv_heads * tiles * sizeof(float);
-  return kStatusBytes + ((bytes + 255) & ~size_t(255));
+  return (bytes + 255) & ~size_t(255);
+}
+
+size_t attn_fwd_workspace_size_for(int32_t batch, int32_t kv_heads, int64_t num_keys, int32_t head_dim) {
+  if (batch < 0 || kv_heads < 0 || num_keys < 0 || head_dim <= 0) return 0;
+  if (head_dim != 64 && head_dim != 128) return kStatusBytes;  // no tensor-core kernel: the status word only
+  const size_t parts = (split_partial_bytes(head_dim) + 255) & ~size_t(255);
+  return kStatusBytes + key_bound_bytes(batch, kv_heads, num_keys, head_dim) + parts;
 }
 size_t kv_append_workspace_size(void) { return kStatusBytes; }
 
@@ -182,6 +189,8 @@ static attn_status attn_fwd_impl(const attn_tensor* q, const attn_tensor* k, con
   a.mask_stride = mask_stride_b;
   a.key_lens = key_lens;
   a.key_bound = nullptr;
+  a.part_ws = nullptr;
+  a.part_bytes = 0;
   a.scale = scale;
   a.lse = lse;
   a.status = static_cast<uint32_t*>(workspace);
@@ -195,11 +204,18 @@ static attn_status attn_fwd_impl(const attn_tensor* q, const attn_tensor* k, con
     // (one read of K and a launch) pays only on calls of a few hundred
     // microseconds and up: from B Hq Pq Pk D = 2^36 on.
     const double work = static_cast<double>(B) * Hq * static_cast<double>(Pq) * static_cast<double>(Pk) * D;
-    if (D == 64 && work >= 68719476736.0 &&
-        workspace_bytes >= attn_fwd_workspace_size_for(static_cast<int32_t>(B), static_cast<int32_t>(Hkv), Pk,
-                                                       static_cast<int32_t>(D))) {
-      a.key_bound = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
-      if ((st = from_cuda(launch_key_tile_bound(a, stream))) != ATTN_OK) return st;
+    const bool room = workspace_bytes >= attn_fwd_workspace_size_for(static_cast<int32_t>(B),
+                                                                     static_cast<int32_t>(Hkv), Pk,
+                                                                     static_cast<int32_t>(D));
+    if (room) {
+      const size_t kb = key_bound_bytes(static_cast<int32_t>(B), static_cast<int32_t>(Hkv), Pk,
+                                        static_cast<int32_t>(D));
+      a.part_ws = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes + kb);
+      a.part_bytes = workspace_bytes - kStatusBytes - kb;
+      if (D == 64 && work >= 68719476736.0) {
+        a.key_bound = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
+        if ((st = from_cuda(launch_key_tile_bound(a, stream))) != ATTN_OK) return st;
+      }
     }
     return from_cuda(launch_attn_fwd_tc(a, stream));
   }

@@ -125,6 +125,16 @@ struct TcParams {
   const int32_t* key_lens;  // per-batch valid keys, or null (all Pk)
   const float* key_bound;   // [B, Hkv, key_tiles] largest |k| element per 128-key tile, or null
   int key_tiles;
+  // Non-paged grids are 1-D over units (query-tile pair, head, batch), the
+  // pair fastest.  The first full_units CTAs take one unit each; the rest
+  // take one of `split` parts of the KV tiles of the remaining units, so the
+  // last wave fills every SM.  A part writes its rows (normalised, f32) and
+  // LSE (natural log) to part_o / part_lse for split_merge_kernel.
+  int nq;  // query-tile pairs per (batch, head)
+  int full_units;
+  int split;
+  float* part_o;    // [units past full_units][split][2 kBM][D]
+  float* part_lse;  // [units past full_units][split][2 kBM]
   // PAGED: cache read through the block table
   const int32_t* bt;
   int64_t bt_stride;
@@ -138,6 +148,47 @@ struct TcParams {
   uint32_t* status;
   TmaCoordMap cq, ck, cv;
 };
+
+// Which (query-tile pair, head, batch) a CTA works on, and which KV part.
+struct UnitIdx {
+  int h, b, q0;
+  int part;   // >= 0: index of this CTA's KV part of a split unit
+  int prow0;  // first row of that part in part_o / part_lse
+};
+
+template <bool PAGED>
+__device__ __forceinline__ UnitIdx unit_index(const TcParams& prm, unsigned bx, unsigned by, unsigned bz,
+                                              unsigned gx) {
+  UnitIdx u;
+  u.part = -1;
+  u.prow0 = 0;
+  if constexpr (PAGED) {
+    u.h = static_cast<int>(by);
+    u.b = static_cast<int>(bz);
+    // causal: the longest query tiles (latest positions) first
+    u.q0 = static_cast<int>(prm.causal ? gx - 1 - bx : bx) * (2 * kBM);
+  } else {
+    int unit = static_cast<int>(bx);
+    if (unit >= prm.full_units) {
+      const int r = unit - prm.full_units;
+      unit = prm.full_units + r / prm.split;
+      u.part = r % prm.split;
+      u.prow0 = r * (2 * kBM);
+    }
+    u.q0 = (unit % prm.nq) * (2 * kBM);
+    u.h = (unit / prm.nq) % prm.Hq;
+    u.b = unit / (prm.nq * prm.Hq);
+  }
+  return u;
+}
+
+// The CTA index read through an opaque move, so that a unit decoded from it
+// is recomputed where it is needed rather than kept live in registers.
+__device__ __forceinline__ unsigned cta_x() {
+  unsigned x;
+  asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(x));
+  return x;
+}
 
 __device__ __forceinline__ void coords(const TmaCoordMap& m, int p, int h, int b, int& c1, int& c2, int& c3) {
   c1 = m.slot_p == 1 ? p : (m.slot_h == 1 ? h : b);
@@ -159,16 +210,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
-  const int b = blockIdx.z;
+  const UnitIdx ui = unit_index<PAGED>(prm, blockIdx.x, blockIdx.y, blockIdx.z, gridDim.x);
+  const int h = ui.h, b = ui.b, q0 = ui.q0;
   const int g = h / prm.group;
   // keys of this batch row: all Pk, or its valid length (tiles past it are skipped)
-  int q0 = blockIdx.x * (2 * kBM);
   int n_keys = prm.Pk;
   int start = 0;  // PAGED: position of the chunk's first token
   if constexpr (PAGED) {
-    // causal: the longest query tiles (latest positions) first
-    if (prm.causal) q0 = (gridDim.x - 1 - blockIdx.x) * (2 * kBM);
     start = prm.start_pos[b];
     const int64_t seq_len = static_cast<int64_t>(start) + prm.Pq;
     if (start < 0 || seq_len > static_cast<int64_t>(prm.max_blocks) * 16) {
@@ -182,7 +230,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int len = prm.key_lens[b];
     n_keys = len < 0 ? 0 : (len < prm.Pk ? len : prm.Pk);
   }
-  const int nkv = (n_keys + kBN - 1) / kBN;
+  // this CTA's key tiles: [kv0, kv0 + nkv), all of them unless it is a part
+  int kv0 = 0;
+  int nkv = (n_keys + kBN - 1) / kBN;
+  if (ui.part >= 0) {
+    const int per = (nkv + prm.split - 1) / prm.split;
+    kv0 = min(nkv, ui.part * per);
+    nkv = min(nkv, kv0 + per) - kv0;
+  }
   volatile int* abort = &bars->abort;
 
   if (threadIdx.x == 0) {
@@ -244,8 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the tile's keys sit in logical blocks 8j .. 8j+7; blocks wholly
           // past the CTA's last key are not loaded, nor is a bad block id
           constexpr int kBlk = kBN / 16;
-          const int nb = min(kBlk, (n_keys - j * kBN + 15) / 16);
-          const int32_t* row = prm.bt + static_cast<int64_t>(b) * prm.bt_stride + j * kBlk;
+          const int nb = min(kBlk, (n_keys - (kv0 + j) * kBN + 15) / 16);
+          const int32_t* row = prm.bt + static_cast<int64_t>(b) * prm.bt_stride + (kv0 + j) * kBlk;
           int ids[kBlk];
           int n_ok = 0;
 #pragma unroll
@@ -285,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           if (!mbar_wait(&bars->k_empty[s], ph ^ 1, abort, prm.status)) break;
           mbar_arrive_expect_tx(&bars->k_full[s], C::kTileBytes);
-          coords(prm.ck, j * kBN, g, b, c1, c2, c3);
+          coords(prm.ck, (kv0 + j) * kBN, g, b, c1, c2, c3);
 #pragma unroll
           for (int x = 0; x < C::kBoxes; ++x)
             tma_load_4d(smem + C::kOffK + s * C::kTileBytes + x * kBoxBytes, &tm_k, &bars->k_full[s], x * 64,
@@ -293,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           k_issued = j + 1;
           if (!mbar_wait(&bars->v_empty[s], ph ^ 1, abort, prm.status)) break;
           mbar_arrive_expect_tx(&bars->v_full[s], C::kTileBytes);
-          coords(prm.cv, j * kBN, g, b, c1, c2, c3);
+          coords(prm.cv, (kv0 + j) * kBN, g, b, c1, c2, c3);
 #pragma unroll
           for (int x = 0; x < C::kBoxes; ++x)
             tma_load_4d(smem + C::kOffV + s * C::kTileBytes + x * kBoxBytes, &tm_v, &bars->v_full[s], x * 64,
@@ -445,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool any = false;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int key = j * kBN + lane * 4 + e;
+        const int key = (kv0 + j) * kBN + lane * 4 + e;
         v[e] = key >= n_keys ? -INFINITY : (mrow ? mrow[key] * kLog2e : 0.0f);
         any |= v[e] != 0.0f;
       }
@@ -458,7 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // softmax skip its max pass.
         if (lane == 0)
           bars->kmax[s] = prm.key_bound != nullptr
-                              ? prm.key_bound[(static_cast<int64_t>(b) * (prm.Hq / prm.group) + g) * prm.key_tiles + j]
+                              ? prm.key_bound[(static_cast<int64_t>(b) * (prm.Hq / prm.group) + g) * prm.key_tiles +
+                                              kv0 + j]
                               : INFINITY;
       }
       __syncwarp();
@@ -514,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_addr + s_col + c * 32, sr[c]);
       // keys of this tile the row may see: [0, lim)
-      const int lim = row_lim - j * kBN;
+      const int lim = row_lim - (kv0 + j) * kBN;
       const bool masked_tile = PAGED ? __any_sync(0xffffffffu, lim < kBN) || !prm.scale_positive
                                      : bars->m_flag[mb_i] != 0;
 #pragma unroll
@@ -712,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // whatever the cache's unfilled slots hold); zero them before PV reads
         // them.  Both softmax warpgroups write the same zeros.  The stage is
         // not refilled before this warpgroup's p_full below.
-        const int r0 = n_keys - j * kBN;
+        const int r0 = n_keys - (kv0 + j) * kBN;
         if (j == nkv - 1 && r0 < kBN) {
           const int s = j % C::kStages;
           if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_full[s], (j / C::kStages) & 1, abort, prm.status))) {
@@ -740,11 +796,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_final[t], 0, abort, prm.status));
       tc_fence_after();
     }
-    const int qi = q0 + t * kBM + row;
+    // the unit again, from the CTA index (cheaper than keeping it live)
+    const UnitIdx ue = unit_index<PAGED>(prm, PAGED ? blockIdx.x : cta_x(), blockIdx.y, blockIdx.z, gridDim.x);
+    const int part = ue.part;
+    const int qi = ue.q0 + t * kBM + row;
     const bool empty = !(l_run > 0.0f);
     const float inv_l = empty ? 0.0f : 1.0f / l_run;
-    const int64_t obase = static_cast<int64_t>(b) * prm.out_stride[0] + static_cast<int64_t>(h) * prm.out_stride[1] +
-                          static_cast<int64_t>(qi) * prm.out_stride[2];
+    const int64_t prow = ue.prow0 + t * kBM + row;  // part rows: normalised f32 partials
+    const int64_t obase = part >= 0 ? prow * D
+                                    : static_cast<int64_t>(ue.b) * prm.out_stride[0] +
+                                          static_cast<int64_t>(ue.h) * prm.out_stride[1] +
+                                          static_cast<int64_t>(qi) * prm.out_stride[2];
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t o[32];
@@ -755,7 +817,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = 0u;
       }
-      if (qi < prm.Pq && ok) {
+      if (qi < prm.Pq && ok && part >= 0) {
+        float4* dst = reinterpret_cast<float4*>(prm.part_o + obase + c * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          dst[i] = make_float4(__uint_as_float(o[4 * i + 0]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                               __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+      } else if (qi < prm.Pq && ok) {
         if constexpr (OUT_BF16) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(prm.out) + obase + c * 32);
 #pragma unroll
@@ -776,9 +844,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (prm.lse != nullptr && qi < prm.Pq && ok) {
+    if (qi < prm.Pq && ok && (part >= 0 || prm.lse != nullptr)) {
       const float lse2 = empty ? -INFINITY : (m_run + __log2f(l_run));
-      prm.lse[(static_cast<int64_t>(b) * prm.Hq + h) * prm.Pq + qi] = lse2 * 0.6931471805599453f;
+      if (part >= 0)
+        prm.part_lse[prow] = lse2 * 0.6931471805599453f;
+      else
+        prm.lse[(static_cast<int64_t>(ue.b) * prm.Hq + ue.h) * prm.Pq + qi] = lse2 * 0.6931471805599453f;
     }
   }
 
@@ -874,6 +945,56 @@ bool make_cache_map(CUtensorMap* map, void* base, int64_t num_blocks, int Hkv, i
   return r == CUDA_SUCCESS;
 }
 
+// Merge the KV parts of each split unit: per query row, the LSE rule of the
+// ring-attention page (out = sum_c exp(lse_c - lse) out_c) over its `split`
+// normalised partials.  One warp per row.
+template <int D, bool OUT_BF16>
+__global__ void split_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse, int split,
+                                   int full_units, int tail, int nq, int Hq, int Pq, void* out, int64_t os0,
+                                   int64_t os1, int64_t os2, float* lse) {
+  constexpr int E = D / 32;
+  const int w = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (w >= tail * 2 * kBM) return;
+  const int u = w / (2 * kBM), r = w % (2 * kBM);
+  const int unit = full_units + u;
+  const int qi = (unit % nq) * (2 * kBM) + r;
+  if (qi >= Pq) return;
+  const int h = (unit / nq) % Hq, b = unit / (nq * Hq);
+  float M = -INFINITY;
+  for (int c = 0; c < split; ++c) M = fmaxf(M, part_lse[static_cast<int64_t>(u * split + c) * (2 * kBM) + r]);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.0f;
+  float wsum = 0.0f;
+  if (M != -INFINITY) {
+    for (int c = 0; c < split; ++c) {
+      const int64_t prow = static_cast<int64_t>(u * split + c) * (2 * kBM) + r;
+      const float l = part_lse[prow];
+      if (l == -INFINITY) continue;
+      const float wt = expf(l - M);
+      wsum += wt;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(wt, part_o[prow * D + lane * E + e], acc[e]);
+    }
+  }
+  const bool empty = !(wsum > 0.0f);
+  const float inv = empty ? 0.0f : 1.0f / wsum;
+  const int64_t ob = static_cast<int64_t>(b) * os0 + static_cast<int64_t>(h) * os1 + static_cast<int64_t>(qi) * os2 +
+                     lane * E;
+  if constexpr (OUT_BF16) {
+    uint16_t* dst = static_cast<uint16_t*>(out) + ob;
+#pragma unroll
+    for (int e = 0; e < E; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+  } else {
+    float* dst = static_cast<float*>(out) + ob;
+#pragma unroll
+    for (int e = 0; e < E; ++e) dst[e] = acc[e] * inv;
+  }
+  if (lse != nullptr && lane == 0)
+    lse[(static_cast<int64_t>(b) * Hq + h) * Pq + qi] = empty ? -INFINITY : M + logf(wsum);
+}
+
 template <int D, bool OUT_BF16>
 cudaError_t launch_tc(const AttnFwdArgs& a, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
@@ -897,13 +1018,44 @@ cudaError_t launch_tc(const AttnFwdArgs& a, cudaStream_t stream) {
   p.out_stride[2] = a.out.stride[2];
   p.lse = a.lse;
   p.status = a.status;
+  // One CTA per unit (query-tile pair, head, batch); when the units end in a
+  // partial wave, the units of that wave are each split into parts over
+  // their KV tiles so that the last wave fills the SMs, and merged after.
+  const int64_t nq = (a.Pq + 2 * kBM - 1) / (2 * kBM);
+  const int64_t units = nq * a.Hq * a.B;
+  if (units > 0x7fffffff / 8) return cudaErrorInvalidValue;
+  p.nq = static_cast<int>(nq);
+  p.full_units = static_cast<int>(units);
+  p.split = 1;
+  p.part_o = a.part_ws;
+  p.part_lse = nullptr;
+  const int sms = device_sm_count();
+  const int64_t tail = sms > 0 ? units % sms : 0;
+  if (a.part_ws != nullptr && units > sms && tail > 0 && tail <= sms / 2) {
+    const int64_t kv_tiles = (a.Pk + kBN - 1) / kBN;
+    int split = static_cast<int>(sms / tail);
+    split = split > 8 ? 8 : split;
+    if (split > kv_tiles / 2) split = static_cast<int>(kv_tiles / 2);
+    const size_t rows = static_cast<size_t>(tail) * split * (2 * kBM);
+    if (split >= 2 && rows * (D + 1) * sizeof(float) <= a.part_bytes) {
+      p.full_units = static_cast<int>(units - tail);
+      p.split = split;
+      p.part_lse = a.part_ws + rows * D;
+    }
+  }
   auto kern = attn_fwd_tc_kernel<D, OUT_BF16, false>;
   const int smem = Cfg<D>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>((a.Pq + 2 * kBM - 1) / (2 * kBM)), static_cast<unsigned>(a.Hq),
-            static_cast<unsigned>(a.B));
-  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, p);
+  const int64_t ctas = p.full_units + (units - p.full_units) * p.split;
+  kern<<<static_cast<unsigned>(ctas), kThreads, smem, stream>>>(mq, mk, mv, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.split == 1) return e;
+  const int tail_units = static_cast<int>(units - p.full_units);
+  const int64_t threads = static_cast<int64_t>(tail_units) * (2 * kBM) * 32;
+  split_merge_kernel<D, OUT_BF16><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
+      p.part_o, p.part_lse, p.split, p.full_units, tail_units, p.nq, p.Hq, p.Pq, a.out.data, a.out.stride[0],
+      a.out.stride[1], a.out.stride[2], a.lse);
   return cudaGetLastError();
 }
 
@@ -943,6 +1095,24 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+int device_sm_count() {
+  static int counts[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (counts[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    counts[dev] = n;
+  }
+  return counts[dev];
+}
+
+size_t split_partial_bytes(int D) {
+  // at most one SM's worth of part CTAs per SM, each 2 kBM rows of D + 1 floats
+  const size_t sms = static_cast<size_t>(device_sm_count());
+  return sms * (2 * kBM) * (static_cast<size_t>(D) + 1) * sizeof(float);
+}
 
 cudaError_t launch_attn_fwd_tc(const AttnFwdArgs& a, cudaStream_t stream) {
   const bool bf16_out = a.out.dtype == ATTN_BF16;

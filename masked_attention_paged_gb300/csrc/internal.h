@@ -23,6 +23,8 @@ struct AttnFwdArgs {
   int64_t mask_stride;
   const int32_t* key_lens;  // [B] valid keys per batch row (keys past it are padding); may be null
   float* key_bound;         // [B, Hkv, ceil(Pk/128)] largest |k| element per key tile, or null
+  float* part_ws;           // room for split-unit partials (tensor-core path), or null
+  size_t part_bytes;
   float scale;
   float* lse;         // [B, Hq, Pq] contiguous, may be null
   uint32_t* status;   // device status word
@@ -37,6 +39,11 @@ cudaError_t launch_attn_empty_keys(const AttnFwdArgs& a, cudaStream_t stream);
 // a.key_bound[(b * Hkv + g) * tiles + j] = max |k| over keys [128 j, 128 j + 128) of (b, g)
 cudaError_t launch_key_tile_bound(const AttnFwdArgs& a, cudaStream_t stream);
 constexpr int kKeyTile = 128;  // keys per tile of the tensor-core kernel
+constexpr int kMaxSplitRows = 256;  // query rows per tensor-core CTA
+// streaming multiprocessors of the current device (cached per device)
+int device_sm_count();
+// bytes of split-unit partials the tensor-core kernel may need for head dim D
+size_t split_partial_bytes(int D);
 
 struct MergeArgs {
   int n;

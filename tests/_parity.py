@@ -43,8 +43,10 @@ def assert_lse_close(gpu, ref, what="lse"):
 
 def sample_rows(B, H, P, n, seed):
     """Seeded query rows (flat ids (b*H + h)*P + i) that always include the
-    first and last row of the first and last head, plus random ones."""
+    first and last row of the first and last head and two rows late in the
+    last head (where the last wave's query tiles sit), plus random ones."""
     rng = np.random.default_rng(seed)
-    fixed = [0, P - 1, (B * H - 1) * P, B * H * P - 1]
+    last = (B * H - 1) * P
+    fixed = [0, P - 1, last, B * H * P - 1, last + (9 * P) // 10, last + (19 * P) // 20]
     rnd = rng.choice(B * H * P, size=max(0, n - len(fixed)), replace=False)
     return np.unique(np.concatenate([np.array(fixed), rnd]).astype(np.int64))

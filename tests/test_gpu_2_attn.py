@@ -151,6 +151,23 @@ def test_key_bound_path_at_its_threshold(gain):
     assert_lse_close(l.reshape(-1)[torch.from_numpy(rows).to(DEV)], rl)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_last_wave_split_over_key_tiles(D):
+    """160 query-tile pairs on a GPU of fewer SMs: the units of the last,
+    partial wave are each split over their key tiles and merged through the
+    LSE; every output element against the oracle (ragged keys, padding and
+    GQA included)."""
+    inp = workloads.make_attn(1, 160, 32, 200, 1000, D, dtype=torch.bfloat16, n_pad=77, seed=44)
+    o, l = _run(inp, bounds=True)
+    ro, rl = oracle.attn(inp.q, inp.k, inp.v, inp.mask, inp.scale)
+    assert_out_close(o, ro, what=f"split D={D}")
+    assert_lse_close(l, rl, what=f"split lse D={D}")
+    # and the same through the bare status-word workspace (no split)
+    o2, l2 = _run(inp, bounds=False)
+    assert (o2.float() - o.float()).abs().max().item() <= 2e-2
+    assert (l2 - l).abs().max().item() <= 1e-3
+
+
 def test_patch_small_workload_full():
     """B1 H16 P1944 D64 bf16 with a seeded 0-64 padded tail: every element."""
     inp = workloads.make_attn_inputs(workloads.ATTN_CONFIGS["patch_small"], seed=0)
