@@ -277,57 +277,115 @@ def timed_steps(step, K, W):
 
 
 def e2e_steps(step, K, W):
-    """The same step through the public API with host buffers: the step's inputs
-    are copied from pinned host memory and its results read back every step
-    (the KV cache and block table are persistent device state)."""
+    """The same step through the public API with host buffers: every step copies
+    its inputs from pinned host memory and reads its results back (the KV
+    cache and block table are persistent device state).  The copies run on
+    their own streams, double-buffered across steps and ordered by events:
+    a call waits only for its own inputs, a result is read back as soon as
+    its call has finished, and a buffer set is refilled only once the step
+    two back is done with it -- so copies overlap computation, and every
+    copied byte is inside the timed region."""
     lib = step.lib
     dev = step.dev
     pin = lambda t: t.contiguous().pin_memory()
-    hs = {"s_q": pin(step.small.q), "s_k": pin(step.small.k), "s_v": pin(step.small.v), "s_m": pin(step.small.mask),
-          "c_q": pin(step.chunk.packed_q), "c_k": pin(step.chunk.packed_k), "c_v": pin(step.chunk.packed_v),
-          "l_q": pin(step.large.q), "l_k": pin(step.large.k), "l_v": pin(step.large.v), "l_m": pin(step.large.mask),
-          "d_q": pin(step.dec.q), "d_kn": pin(step.dec.k_new), "d_vn": pin(step.dec.v_new), "d_pos": pin(step.dec.pos),
-          "d_len": pin(step.dec.ctx_lens)}
+    groups = [  # input groups in call order
+        {"s_q": pin(step.small.q), "s_k": pin(step.small.k), "s_v": pin(step.small.v), "s_m": pin(step.small.mask),
+         "d_q": pin(step.dec.q), "d_kn": pin(step.dec.k_new), "d_vn": pin(step.dec.v_new),
+         "d_pos": pin(step.dec.pos), "d_len": pin(step.dec.ctx_lens)},
+        {"c_q": pin(step.chunk.packed_q), "c_k": pin(step.chunk.packed_k), "c_v": pin(step.chunk.packed_v)},
+        {"l_q": pin(step.large.q), "l_k": pin(step.large.k), "l_v": pin(step.large.v), "l_m": pin(step.large.mask)},
+    ]
     res = {"s_o": torch.empty(step.s_o.shape, dtype=step.s_o.dtype).pin_memory(),
+           "d_o": torch.empty(step.d_o.shape, dtype=step.d_o.dtype).pin_memory(),
            "c_o": torch.empty(step.c_out.shape, dtype=step.c_out.dtype).pin_memory(),
-           "l_o": torch.empty(step.l_o.shape, dtype=step.l_o.dtype).pin_memory(),
-           "d_o": torch.empty(step.d_o.shape, dtype=step.d_o.dtype).pin_memory()}
-    h2d = sum(t.numel() * t.element_size() for t in hs.values())
+           "l_o": torch.empty(step.l_o.shape, dtype=step.l_o.dtype).pin_memory()}
+    h2d = sum(t.numel() * t.element_size() for g in groups for t in g.values())
     d2h = sum(t.numel() * t.element_size() for t in res.values())
-    dbuf = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in hs.items()}
     sc = step.chunk
+    H, T, D = sc.cfg.Hq, sc.cfg.Pq, sc.cfg.D
 
-    def one():
-        for k, v in hs.items():
-            dbuf[k].copy_(v, non_blocking=True)
-        lib.attn_fwd(dbuf["s_q"], dbuf["s_k"], dbuf["s_v"], dbuf["s_m"], step.small.scale, out=step.s_o,
-                     lse=step.s_l, workspace=step.ws_attn)
-        lib.kv_append(step.kc, step.vc, step.bt, dbuf["d_pos"], dbuf["d_kn"], dbuf["d_vn"], workspace=step.ws_dec)
-        lib.paged_decode_attn(dbuf["d_q"], step.kc, step.vc, step.bt, dbuf["d_len"], step.dec.scale, out=step.d_o,
+    def out_set():
+        return {"s_o": torch.empty_like(step.s_o), "s_l": torch.empty_like(step.s_l),
+                "d_o": torch.empty_like(step.d_o),
+                "c_parts": [torch.empty_like(x) for x in step.c_parts],
+                "c_lses": [torch.empty_like(x) for x in step.c_lses],
+                "c_out": torch.empty_like(step.c_out), "c_lse": torch.empty_like(step.c_lse),
+                "l_o": torch.empty_like(step.l_o), "l_l": torch.empty_like(step.l_l)}
+    ins = [[{k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in g.items()} for g in groups]
+           for _ in range(2)]
+    outs = [out_set(), out_set()]
+    cs = torch.cuda.current_stream(dev)
+    hs = torch.cuda.Stream(dev)
+    ds = torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    inputs_free = [None, None]   # compute of the step two back is done with this input set
+    outputs_free = [None, None]  # read-back of the step two back is done with this output set
+
+    def one(i):
+        di, do = ins[i], outs[i]
+        got = []
+        with torch.cuda.stream(hs):
+            if inputs_free[i] is not None:
+                hs.wait_event(inputs_free[i])
+            for g, dg in zip(groups, di):
+                for k, v in g.items():
+                    dg[k].copy_(v, non_blocking=True)
+                e = ev()
+                e.record(hs)
+                got.append(e)
+        if outputs_free[i] is not None:
+            cs.wait_event(outputs_free[i])
+        d0, d1, d2 = di
+        cs.wait_event(got[0])
+        lib.attn_fwd(d0["s_q"], d0["s_k"], d0["s_v"], d0["s_m"], step.small.scale, out=do["s_o"], lse=do["s_l"],
+                     workspace=step.ws_attn)
+        lib.kv_append(step.kc, step.vc, step.bt, d0["d_pos"], d0["d_kn"], d0["d_vn"], workspace=step.ws_dec)
+        lib.paged_decode_attn(d0["d_q"], step.kc, step.vc, step.bt, d0["d_len"], step.dec.scale, out=do["d_o"],
                               workspace=step.ws_dec)
-        q = dbuf["c_q"].permute(1, 0, 2).unsqueeze(0)
-        k = dbuf["c_k"].permute(1, 0, 2).unsqueeze(0)
-        v = dbuf["c_v"].permute(1, 0, 2).unsqueeze(0)
-        for i, (lo, hi) in enumerate(sc.cfg.chunk_bounds()):
-            lib.attn_fwd(q, k[:, :, lo:hi], v[:, :, lo:hi], None, sc.scale, out=step.c_parts[i],
-                         lse=step.c_lses[i], workspace=step.ws_attn)
-        lib.attn_lse_merge(step.c_parts, step.c_lses, out=step.c_out.permute(1, 0, 2).unsqueeze(0), lse=step.c_lse)
-        lib.attn_fwd(dbuf["l_q"], dbuf["l_k"], dbuf["l_v"], dbuf["l_m"], step.large.scale, out=step.l_o,
-                     lse=step.l_l, workspace=step.ws_attn)
-        res["s_o"].copy_(step.s_o, non_blocking=True)
-        res["c_o"].copy_(step.c_out, non_blocking=True)
-        res["l_o"].copy_(step.l_o, non_blocking=True)
-        res["d_o"].copy_(step.d_o, non_blocking=True)
+        done_a = ev()
+        done_a.record(cs)
+        cs.wait_event(got[1])
+        q = d1["c_q"].permute(1, 0, 2).unsqueeze(0)
+        k = d1["c_k"].permute(1, 0, 2).unsqueeze(0)
+        v = d1["c_v"].permute(1, 0, 2).unsqueeze(0)
+        for j, (lo, hi) in enumerate(sc.cfg.chunk_bounds()):
+            lib.attn_fwd(q, k[:, :, lo:hi], v[:, :, lo:hi], None, sc.scale, out=do["c_parts"][j],
+                         lse=do["c_lses"][j], workspace=step.ws_attn)
+        lib.attn_lse_merge(do["c_parts"], do["c_lses"], out=do["c_out"].permute(1, 0, 2).unsqueeze(0),
+                           lse=do["c_lse"])
+        done_b = ev()
+        done_b.record(cs)
+        cs.wait_event(got[2])
+        lib.attn_fwd(d2["l_q"], d2["l_k"], d2["l_v"], d2["l_m"], step.large.scale, out=do["l_o"], lse=do["l_l"],
+                     workspace=step.ws_attn)
+        done_c = ev()
+        done_c.record(cs)
+        inputs_free[i] = done_c
+        with torch.cuda.stream(ds):
+            ds.wait_event(done_a)
+            res["s_o"].copy_(do["s_o"], non_blocking=True)
+            res["d_o"].copy_(do["d_o"], non_blocking=True)
+            ds.wait_event(done_b)
+            res["c_o"].copy_(do["c_out"], non_blocking=True)
+            ds.wait_event(done_c)
+            res["l_o"].copy_(do["l_o"], non_blocking=True)
+            e = ev()
+            e.record(ds)
+            outputs_free[i] = e
 
-    for _ in range(W):
-        one()
+    for w in range(W):
+        one(w % 2)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.perf_counter()
-    e0.record()
-    for _ in range(K):
-        one()
-    e1.record()
+    e0.record(cs)
+    hs.wait_event(e0)
+    ds.wait_event(e0)
+    for s in range(K):
+        one(s % 2)
+    for e in outputs_free:
+        cs.wait_event(e)
+    e1.record(cs)
     torch.cuda.synchronize()
     wall = time.perf_counter() - t0
     ms = max(e0.elapsed_time(e1), wall * 1e3) / K
@@ -553,7 +611,7 @@ def main():
     if not args.no_next:
         line["next"] = next_rows(step, max(5, args.steps // 2), max(3, args.warmup), pk)
     if not args.no_e2e:
-        e_ms, h2d, d2h = e2e_steps(step, max(3, args.steps // 4), 2)
+        e_ms, h2d, d2h = e2e_steps(step, max(5, args.steps // 2), 2)
         e_ms = max_over_ranks(e_ms, world)
         line["e2e"] = {"value": world * step.step_flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
