@@ -208,8 +208,9 @@ class Step:
         self.decode_bytes = (self.kv_bytes + 2 * d.cfg.B * d.cfg.Hq * d.cfg.D * 2 +
                              int(((d.ctx_lens.to(torch.int64) + 15) // 16).sum()) * 4)
         self.merge_bytes = 3 * T * H * D * 2 + 3 * H * T * 4
-        # attn x4 (+ the key-bound pass of the two D=64 calls), append, decode split + reduce, merge
-        self.launches_per_step = 10
+        # attn x4, the P32000 key-bound pass, the last-wave merge of the chunk and P32000 launches (3),
+        # append, decode split + reduce, merge (152-SM GPU: the chunk and P32000 grids end in partial waves)
+        self.launches_per_step = 12
         self.decode_ms_ref = None  # bf16 append + decode time of the step, for the INT8 comparison
 
     @property
@@ -461,7 +462,7 @@ def next_rows(step, K, W, pk):
                                  "ms": q_ms, "gbs": q8_bytes / (q_ms * 1e-3) / 1e9,
                                  "frac": q8_bytes / (q_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
                                  "speedup_vs_bf16_decode": (step.decode_ms_ref / q_ms) if step.decode_ms_ref else None,
-                                 "launches": 3, "bytes": q8_bytes},
+                                 "launches": 3, "bytes": q8_bytes, "traffic": traffic("paged_decode_kernel_q8")},
         "paged_prefill_attn": {"workload": "prefill_chunk (16 seqs x 1024-token causal chunk after U[0, 7168] "
                                            "cached, Hq 32, Hkv 8, D 128)",
                                "ms": p_ms, "tflops": p_tf, "frac": p_tf / peak_t, "launches": 2,
