@@ -945,6 +945,17 @@ bool make_cache_map(CUtensorMap* map, void* base, int64_t num_blocks, int Hkv, i
   return r == CUDA_SUCCESS;
 }
 
+// The setmaxnreg split (the control warpgroup down to 88 registers, the two
+// softmax warpgroups up to 208) must fit in the registers the launch gives
+// the CTA (threads x registers per thread as compiled); a split that asks for
+// more would wait forever, so a kernel compiled with fewer is never launched.
+template <typename Kern>
+bool register_split_fits(Kern kern) {
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return false;
+  return 128 * 88 + 256 * 208 <= fa.numRegs * kThreads;
+}
+
 // Merge the KV parts of each split unit: per query row, the LSE rule of the
 // ring-attention page (out = sum_c exp(lse_c - lse) out_c) over its `split`
 // normalised partials.  One warp per row.
@@ -1044,6 +1055,8 @@ cudaError_t launch_tc(const AttnFwdArgs& a, cudaStream_t stream) {
     }
   }
   auto kern = attn_fwd_tc_kernel<D, OUT_BF16, false>;
+  static const bool regs_fit = register_split_fits(kern);
+  if (!regs_fit) return cudaErrorInvalidConfiguration;
   const int smem = Cfg<D>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -1085,6 +1098,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.lse = a.lse;
   p.status = a.status;
   auto kern = attn_fwd_tc_kernel<D, OUT_BF16, true>;
+  static const bool regs_fit = register_split_fits(kern);
+  if (!regs_fit) return cudaErrorInvalidConfiguration;
   const int smem = Cfg<D>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
