@@ -51,6 +51,7 @@
 #include <cuda.h>
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "common.cuh"
@@ -1112,15 +1113,15 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
 }  // namespace
 
 int device_sm_count() {
-  static int counts[64] = {};
+  static std::atomic<int> counts[64] = {};  // per device; any thread may fill an entry (same value)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (counts[dev] == 0) {
-    int n = 0;
+  int n = counts[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    counts[dev] = n;
+    counts[dev].store(n, std::memory_order_relaxed);
   }
-  return counts[dev];
+  return n;
 }
 
 size_t split_partial_bytes(int D) {
