@@ -863,6 +863,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Merge the KV parts of each split unit: per query row, the LSE rule of the
+// ring-attention page (out = sum_c exp(lse_c - lse) out_c) over its `split`
+// normalised partials.  One warp per row.
+template <int D, bool OUT_BF16>
+__global__ void split_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse, int split,
+                                   int full_units, int tail, int nq, int Hq, int Pq, void* out, int64_t os0,
+                                   int64_t os1, int64_t os2, float* lse) {
+  constexpr int E = D / 32;
+  const int w = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (w >= tail * 2 * kBM) return;
+  const int u = w / (2 * kBM), r = w % (2 * kBM);
+  const int unit = full_units + u;
+  const int qi = (unit % nq) * (2 * kBM) + r;
+  if (qi >= Pq) return;
+  const int h = (unit / nq) % Hq, b = unit / (nq * Hq);
+  float M = -INFINITY;
+  for (int c = 0; c < split; ++c) M = fmaxf(M, part_lse[static_cast<int64_t>(u * split + c) * (2 * kBM) + r]);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.0f;
+  float wsum = 0.0f;
+  if (M != -INFINITY) {
+    for (int c = 0; c < split; ++c) {
+      const int64_t prow = static_cast<int64_t>(u * split + c) * (2 * kBM) + r;
+      const float l = part_lse[prow];
+      if (l == -INFINITY) continue;
+      const float wt = expf(l - M);
+      wsum += wt;
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(wt, part_o[prow * D + lane * E + e], acc[e]);
+    }
+  }
+  const bool empty = !(wsum > 0.0f);
+  const float inv = empty ? 0.0f : 1.0f / wsum;
+  const int64_t ob = static_cast<int64_t>(b) * os0 + static_cast<int64_t>(h) * os1 + static_cast<int64_t>(qi) * os2 +
+                     lane * E;
+  if constexpr (OUT_BF16) {
+    uint16_t* dst = static_cast<uint16_t*>(out) + ob;
+#pragma unroll
+    for (int e = 0; e < E; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+  } else {
+    float* dst = static_cast<float*>(out) + ob;
+#pragma unroll
+    for (int e = 0; e < E; ++e) dst[e] = acc[e] * inv;
+  }
+  if (lse != nullptr && lane == 0)
+    lse[(static_cast<int64_t>(b) * Hq + h) * Pq + qi] = empty ? -INFINITY : M + logf(wsum);
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -955,56 +1005,6 @@ bool register_split_fits(Kern kern) {
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return false;
   return 128 * 88 + 256 * 208 <= fa.numRegs * kThreads;
-}
-
-// Merge the KV parts of each split unit: per query row, the LSE rule of the
-// ring-attention page (out = sum_c exp(lse_c - lse) out_c) over its `split`
-// normalised partials.  One warp per row.
-template <int D, bool OUT_BF16>
-__global__ void split_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse, int split,
-                                   int full_units, int tail, int nq, int Hq, int Pq, void* out, int64_t os0,
-                                   int64_t os1, int64_t os2, float* lse) {
-  constexpr int E = D / 32;
-  const int w = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
-  const int lane = threadIdx.x & 31;
-  if (w >= tail * 2 * kBM) return;
-  const int u = w / (2 * kBM), r = w % (2 * kBM);
-  const int unit = full_units + u;
-  const int qi = (unit % nq) * (2 * kBM) + r;
-  if (qi >= Pq) return;
-  const int h = (unit / nq) % Hq, b = unit / (nq * Hq);
-  float M = -INFINITY;
-  for (int c = 0; c < split; ++c) M = fmaxf(M, part_lse[static_cast<int64_t>(u * split + c) * (2 * kBM) + r]);
-  float acc[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.0f;
-  float wsum = 0.0f;
-  if (M != -INFINITY) {
-    for (int c = 0; c < split; ++c) {
-      const int64_t prow = static_cast<int64_t>(u * split + c) * (2 * kBM) + r;
-      const float l = part_lse[prow];
-      if (l == -INFINITY) continue;
-      const float wt = expf(l - M);
-      wsum += wt;
-#pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = fmaf(wt, part_o[prow * D + lane * E + e], acc[e]);
-    }
-  }
-  const bool empty = !(wsum > 0.0f);
-  const float inv = empty ? 0.0f : 1.0f / wsum;
-  const int64_t ob = static_cast<int64_t>(b) * os0 + static_cast<int64_t>(h) * os1 + static_cast<int64_t>(qi) * os2 +
-                     lane * E;
-  if constexpr (OUT_BF16) {
-    uint16_t* dst = static_cast<uint16_t*>(out) + ob;
-#pragma unroll
-    for (int e = 0; e < E; e += 2) *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
-  } else {
-    float* dst = static_cast<float*>(out) + ob;
-#pragma unroll
-    for (int e = 0; e < E; ++e) dst[e] = acc[e] * inv;
-  }
-  if (lse != nullptr && lane == 0)
-    lse[(static_cast<int64_t>(b) * Hq + h) * Pq + qi] = empty ? -INFINITY : M + logf(wsum);
 }
 
 template <int D, bool OUT_BF16>
