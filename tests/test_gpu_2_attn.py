@@ -263,8 +263,9 @@ def test_no_score_matrix_is_allocated():
         extra[P] = torch.cuda.max_memory_allocated() - base
         out_bytes = o.numel() * 2 + l.numel() * 4
         assert extra[P] <= out_bytes + (2 << 20), (P, extra[P], out_bytes)
-        # a single bf16 score matrix H x P x P would be 30x (P=1944) to 180x (P=11616) larger
-        assert extra[P] * 25 < oracle.score_matrix_bytes(16, P, 2)
+        # a single bf16 score matrix H x P x P would be 30x (P=1944) to 180x (P=11616)
+        # larger than out + lse (the allocator's block rounding can add ~1 MB to the peak)
+        assert extra[P] * 20 < oracle.score_matrix_bytes(16, P, 2)
         # nothing outside torch's allocator either (allow allocator granularity)
         assert free0 - free1 <= out_bytes + (64 << 20)
         del o, l

@@ -60,3 +60,23 @@ def test_key_padding_mask_conversion_and_direction():
     inv = lib.key_padding_to_additive((~kpm).cuda())
     o_inv, _ = lib.attn_fwd(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), inv, inp.scale)
     assert (o_inv.float() - o.float()).abs().max().item() > 0.1
+
+
+@pytest.mark.parametrize("D,out_dtype,with_lse", [(64, torch.bfloat16, True), (128, torch.float32, False)])
+def test_varlen_with_a_split_last_wave(D, out_dtype, with_lse):
+    """160 heads: the units of the last wave are split over their key tiles;
+    per-batch key lengths then bound each part's tiles.  f32 output and no
+    LSE buffer go through the same merge."""
+    lens = [700, 129]
+    B, Pk = 2, 700
+    inp = workloads.make_attn(B, 80, 16, 230, Pk, D, dtype=torch.bfloat16, n_pad=[Pk - n for n in lens], seed=35)
+    kl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    ws = lib.Workspace(lib.attn_fwd_workspace_size_for(B, 16, Pk, D))
+    out = torch.empty(inp.q.shape, dtype=out_dtype, device="cuda")
+    res = lib.attn_fwd_varlen(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), kl, inp.scale, out=out, workspace=ws,
+                              return_lse=with_lse)
+    assert ws.status() == 0
+    ro, rl = oracle.attn(inp.q, inp.k, inp.v, inp.mask, inp.scale)
+    assert_out_close(out, ro, fp32_inputs=False)
+    if with_lse:
+        assert_lse_close(res[1], rl)
