@@ -195,7 +195,10 @@ def _small_ws(device) -> Workspace:
 
 def _attn_ws(q: torch.Tensor, k: torch.Tensor) -> Workspace:
     """Default attn_fwd workspace: the status word plus room for the per-tile
-    key bounds of this shape (kept per device, grown when a call needs more)."""
+    key bounds and the last-wave partials of this shape (kept per device,
+    grown when a call needs more).  It is shared by every call on the device
+    that passes no workspace, so calls that may run concurrently (on
+    different streams) must each pass their own."""
     need = attn_fwd_workspace_size_for(k.shape[0], k.shape[1], k.shape[2], k.shape[3])
     key = ("attn", torch.device(q.device).index)
     ws = _default_ws.get(key)
