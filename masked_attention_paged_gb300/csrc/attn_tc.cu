@@ -996,6 +996,23 @@ bool make_cache_map(CUtensorMap* map, void* base, int64_t num_blocks, int Hkv, i
   return r == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+bool make_code_cache_map(CUtensorMap* map, void* base, int64_t num_blocks, int Hkv) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {128, 16, static_cast<cuuint64_t>(Hkv), static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[3] = {128, 16 * 128, static_cast<cuuint64_t>(Hkv) * 16 * 128};
+  const cuuint32_t box[4] = {128, 16, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+namespace {
+
 // The setmaxnreg split (the control warpgroup down to 88 registers, the two
 // softmax warpgroups up to 208) must fit in the registers the launch gives
 // the CTA (threads x registers per thread as compiled); a split that asks for

@@ -493,13 +493,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodeParams& p, cudaStream
   kern<<<grid, kWarps * 32, smem, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t warps = a.B * a.Hq;
-  const unsigned blocks = static_cast<unsigned>((warps * 32 + 127) / 128);
-  decode_reduce_kernel<D><<<blocks, 128, 0, stream>>>(p.o_part, p.lse_part, a.ctx_lens, p.len_add, a.max_blocks * kBS,
-                                                     a.n_split, a.B, static_cast<int>(a.Hq), a.out.data,
-                                                     a.out.dtype == ATTN_BF16, a.out.stride[0], a.out.stride[1],
-                                                     a.lse);
-  return cudaGetLastError();
+  return launch_decode_reduce(a, p.o_part, p.lse_part, p.len_add, stream);
 }
 
 template <int D, bool Q8>
@@ -515,7 +509,21 @@ cudaError_t launch_decode_d(const DecodeArgs& a, const DecodeParams& p, cudaStre
 
 }  // namespace
 
+// host side
+
+cudaError_t launch_decode_reduce(const DecodeArgs& a, const float* o_part, const float* lse_part, int len_add,
+                                 cudaStream_t stream) {
+  const int64_t warps = a.B * a.Hq;
+  const unsigned blocks = static_cast<unsigned>((warps * 32 + 127) / 128);
+  auto kern = a.cache.D == 64 ? decode_reduce_kernel<64> : decode_reduce_kernel<128>;
+  kern<<<blocks, 128, 0, stream>>>(o_part, lse_part, a.ctx_lens, len_add, a.max_blocks * kBS, a.n_split, a.B,
+                                   static_cast<int>(a.Hq), a.out.data, a.out.dtype == ATTN_BF16, a.out.stride[0],
+                                   a.out.stride[1], a.lse);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
+  if (paged_decode_q8_mma_supported(a)) return launch_paged_decode_q8_mma(a, stream);
   DecodeParams p;
   p.kc = a.cache.k;
   p.vc = a.cache.v;

@@ -1,0 +1,475 @@
+// decode_q8.cu -- paged GQA decode over an INT8 KV cache on the tensor cores
+// ("LLM inference memory accounting", section 18: an INT8 cache halves the
+// KV bytes and adds per-token scales and a dequantisation step; "KV cache in
+// nanoVLM": one query token per sequence attends over its cached K/V).
+//
+// Head dim 128, up to 8 query heads per KV head.  The FMA decode spends about
+// eight instructions on every INT8 code (dequantise, then one fp32 multiply
+// per query head), which leaves it issue-bound at half the bytes of the bf16
+// cache.  Here both products run as mma.sync.m16n8k16 (fp16 in, fp32
+// accumulate) and a code costs under one instruction:
+//  * a code c is turned into the fp16 number 1152 + c by one LOP3 that puts
+//    its byte (sign bit flipped, i.e. c + 128) under the exponent of 1024;
+//    the 1152 it carries is removed afterwards: from the scores with the
+//    per-head constant 1152 * sum(q), from the output with 1152 times the
+//    sum of the weights, which a further MMA against a tile of ones yields in
+//    the same rounding as the output;
+//  * scores S = Q K^T with the query heads as the A rows (zero padded) and
+//    the 16 tokens of a block as two n-tiles; the score fragment is, register
+//    for register, the A fragment of the P V product, so no shuffle moves it;
+//  * the key scale multiplies the score; the value scale joins the softmax
+//    weight through a second exponent stream, w = 2^(s + log2 vs - M) with its
+//    own running max M, so the fp16 weights stay in [0, 2^8] whatever the
+//    scales are, and O accumulates straight in the MMA registers;
+//  * each warp streams its blocks with two 4-D TMA loads per block (K and V
+//    codes, 128-byte swizzle) plus two bulk copies of the row scales; tokens
+//    are taken in the order n ^ ((n & 1) << 2) within each group of eight,
+//    which makes every fragment load of K and of V free of bank conflicts.
+// The CTA decomposition, the cross-warp combine and the split merge are those
+// of the FMA decode: split s of 1024 tokens x KV head x sequence per CTA.
+#include <cuda.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace attn {
+namespace {
+
+constexpr int kBS = 16;       // tokens per cache block
+constexpr int kD = 128;       // head dim (one 128-byte code row per token)
+constexpr int kWarps = 4;
+constexpr int kQ8Stages = 3;  // per-warp buffer depth
+constexpr int kCodeBytes = kBS * kD;  // one (block, head) of K or V codes
+constexpr float kLazy = 8.0f;         // log2 headroom before a running max moves
+constexpr float kBias = 1152.0f;      // value carried by the fp16 form of code 0
+constexpr uint32_t kByteMask = 0x00FF00FFu;
+constexpr uint32_t kHalfBits = 0x64806480u;  // exponent of 1024 in each half; 0x80 flips the code's sign bit
+
+struct Q8MmaParams {
+  CUtensorMap kmap;  // codes [num_blocks, Hkv, 16, 128] u8, box = one (block, head)
+  CUtensorMap vmap;
+  const float* ks;   // [num_blocks, Hkv, 16]
+  const float* vs;
+  int64_t num_blocks;
+  int Hkv;
+  int Hq;
+  const uint16_t* q;
+  int64_t q_stride[2];  // batch, head
+  const int32_t* bt;
+  int64_t bt_stride;
+  int max_blocks;
+  const int32_t* ctx_lens;
+  float scale_log2;
+  float* o_part;    // [B, Hq, n_split, D]
+  float* lse_part;  // [B, Hq, n_split], log2 units
+  int n_split;
+  uint32_t* status;
+};
+
+// two codes (bytes 0 and 2 of x) as the fp16 pair (1152 + c0, 1152 + c2):
+// bits under the mask take x with the sign bit flipped, the rest the exponent
+__device__ __forceinline__ uint32_t codes_to_half2(uint32_t x) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(x), "r"(kByteMask), "r"(kHalfBits));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// round-to-nearest-even f32 -> fp16 of two values; `lo` lands in bits 0..15
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// lo + hi of an fp16 pair (both exact in fp32)
+__device__ __forceinline__ float half2_sum(uint32_t x) {
+  float lo, hi;
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(x));
+  return lo + hi;
+}
+
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// D (16x8, fp32) += A (16x16, fp16, rows g and g+8 in a0/a2 and a1/a3) * B (16x8)
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int w) {
+  return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
+}
+
+// token of position n (0..15) in the order the fragments use
+__device__ __forceinline__ int tok_of(int n) { return n ^ ((n & 1) << 2); }
+
+template <int G>
+__global__ void __launch_bounds__(kWarps * 32, 3) paged_decode_q8_mma_kernel(const __grid_constant__ Q8MmaParams p) {
+  static_assert(G >= 1 && G <= 8, "query heads per KV head");
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the swizzled TMA tiles
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* codes = smem;                                                      // [warp][stage][K, V][2048]
+  float* scl = reinterpret_cast<float*>(codes + kWarps * kQ8Stages * 2 * kCodeBytes);  // [warp][stage][K 16, V 16]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(scl + kWarps * kQ8Stages * 2 * kBS);
+  float* comb = reinterpret_cast<float*>(bars + kWarps * kQ8Stages);  // [warp][G][D + 2]
+
+  const int split = blockIdx.x, gkv = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2;  // fragment row: query head of the group (rows >= G are zero)
+  const int t = lane & 3;   // fragment column pair
+  int L = p.ctx_lens[b];
+  L = L < 0 ? 0 : L;
+  if (L > p.max_blocks * kBS) {
+    if (threadIdx.x == 0 && split == 0) report(p.status, kStatusBounds);
+    L = p.max_blocks * kBS;
+  }
+  const int t_begin = split * kDecodeSplitTokens;
+  if (t_begin >= L) return;  // nothing of this sequence in this split
+  const int t_end = min(L, t_begin + kDecodeSplitTokens);
+  const int nblk = (t_end - t_begin + kBS - 1) / kBS;
+  const int lb0 = t_begin / kBS;
+
+  uint8_t* wcodes = codes + warp * kQ8Stages * 2 * kCodeBytes;
+  float* wscl = scl + warp * kQ8Stages * 2 * kBS;
+  uint64_t* wbar = bars + warp * kQ8Stages;
+  if (lane == 0) {
+    for (int s = 0; s < kQ8Stages; ++s) mbar_init(&wbar[s], 1);
+    if (warp == 0) {
+      tma_prefetch_desc(&p.kmap);
+      tma_prefetch_desc(&p.vmap);
+    }
+  }
+  fence_mbar_init();
+  __syncwarp();
+
+  const int my_n = nblk > warp ? (nblk - warp + kWarps - 1) / kWarps : 0;
+  int my_blk = -1;
+  if (lane < my_n) {
+    my_blk = p.bt[static_cast<int64_t>(b) * p.bt_stride + lb0 + warp + kWarps * lane];
+    if (my_blk < 0 || my_blk >= p.num_blocks) {
+      report(p.status, kStatusBounds);
+      my_blk = -1;
+    }
+  }
+  auto issue = [&](int i, int blk) {
+    const int s = i % kQ8Stages;
+    if (blk < 0) {  // bad id: complete the phase without data; the block is skipped
+      mbar_arrive(&wbar[s]);
+      return;
+    }
+    uint8_t* dst = wcodes + s * 2 * kCodeBytes;
+    float* sdst = wscl + s * 2 * kBS;
+    const int64_t row = static_cast<int64_t>(blk) * p.Hkv + gkv;
+    fence_proxy_async_smem();
+    mbar_arrive_expect_tx(&wbar[s], 2 * kCodeBytes + 2 * kBS * 4);
+    tma_load_4d(dst, &p.kmap, &wbar[s], 0, 0, gkv, blk);
+    tma_load_4d(dst + kCodeBytes, &p.vmap, &wbar[s], 0, 0, gkv, blk);
+    bulk_load(sdst, p.ks + row * kBS, kBS * 4, &wbar[s]);
+    bulk_load(sdst + kBS, p.vs + row * kBS, kBS * 4, &wbar[s]);
+  };
+
+  // ---- q of head g as fp16 A fragments.  K chunk c = 4 h + w of the QK
+  // product takes dims d0 = 16 t + 64 h + 4 w .. d0 + 3 in this lane: the
+  // k-slots (2t, 2t+1) hold dims (d0, d0+2), the slots (2t+8, 2t+9) dims
+  // (d0+1, d0+3), matching the byte order codes_to_half2 produces.
+  float qv[32];
+  if (g < G) {
+    const uint16_t* qrow = p.q + b * p.q_stride[0] + (gkv * G + g) * p.q_stride[1];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint4 w0 = *reinterpret_cast<const uint4*>(qrow + 16 * t + 64 * h);
+      const uint4 w1 = *reinterpret_cast<const uint4*>(qrow + 16 * t + 64 * h + 8);
+      const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        qv[16 * h + 2 * e] = bf16lo_to_f32(ws[e]);
+        qv[16 * h + 2 * e + 1] = bf16hi_to_f32(ws[e]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) qv[e] = 0.f;
+  }
+  // a power-of-two prescale keeps q inside the fp16 range (exact; the
+  // scores take the factor back)
+  float qmax = 0.f;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) qmax = fmaxf(qmax, fabsf(qv[e]));
+  qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 1));
+  qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, 2));
+  int qexp = 0;
+  if (qmax >= 32768.f) qexp = static_cast<int>((__float_as_uint(qmax) >> 23) & 0xff) - 127 - 14;
+  const float qpre = __uint_as_float(static_cast<uint32_t>(127 - qexp) << 23);
+  const float sl = p.scale_log2 * __uint_as_float(static_cast<uint32_t>(127 + qexp) << 23);
+  uint32_t qa[8][2];
+  float qsum = 0.f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int e0 = 16 * (c >> 2) + 4 * (c & 3);
+    qa[c][0] = pack_half2(qv[e0] * qpre, qv[e0 + 2] * qpre);
+    qa[c][1] = pack_half2(qv[e0 + 1] * qpre, qv[e0 + 3] * qpre);
+    // the sum of the rounded halves, as the MMA sees them
+    qsum += half2_sum(qa[c][0]) + half2_sum(qa[c][1]);
+  }
+  qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+  qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+  const float corr = kBias * qsum;
+
+  // the four tokens of this lane, in score-fragment order
+  const int T[4] = {tok_of(2 * t), tok_of(2 * t + 1), 8 + tok_of(2 * t), 8 + tok_of(2 * t + 1)};
+  // K fragment rows: token tok_of(g) of each n-tile
+  const int krow = tok_of(g);
+
+  float o[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[j][e] = 0.f;
+  float z[4] = {0.f, 0.f, 0.f, 0.f};
+  float m_run = -INFINITY, w_run = -INFINITY, l_part = 0.f;
+
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) abort_flag = 0;
+  __syncthreads();
+  bool ok = true;
+  int issued = 0;
+  for (int i = 0; i < kQ8Stages && i < my_n; ++i) {
+    const int blk = __shfl_sync(0xffffffffu, my_blk, i);
+    if (lane == 0) issue(i, blk);
+    issued = i + 1;
+  }
+
+  for (int i = 0; i < my_n; ++i) {
+    const int s = i % kQ8Stages;
+    const int blk = __shfl_sync(0xffffffffu, my_blk, i);
+    const bool landed = mbar_wait(&wbar[s], (i / kQ8Stages) & 1, &abort_flag, p.status);
+    if (!__all_sync(0xffffffffu, landed)) {
+      ok = false;
+      break;
+    }
+    if (blk >= 0) {
+      const uint8_t* kb = wcodes + s * 2 * kCodeBytes;
+      const uint8_t* vb = kb + kCodeBytes;
+      const float* ksb = wscl + s * 2 * kBS;
+      const float* vsb = ksb + kBS;
+      const int tok0 = (lb0 + warp + kWarps * i) * kBS;
+
+      // ---- S = Q K^T: n-tile j holds tokens 8 j + tok_of(n)
+      float sacc[2][4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int tok = 8 * j + krow;
+        const uint8_t* rowp = kb + tok * kD;
+        const uint4 k0 = lds128(rowp + ((t ^ krow) << 4));
+        const uint4 k1 = lds128(rowp + (((t + 4) ^ krow) << 4));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[j][e] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t x = word(c < 4 ? k0 : k1, c & 3);
+          mma_f16(sacc[j], qa[c][0], 0u, qa[c][1], 0u, codes_to_half2(x), codes_to_half2(x >> 8));
+        }
+      }
+      // scores in log2 units; the key scale multiplies the dot product with the codes
+      float sc[4] = {sacc[0][0], sacc[0][1], sacc[1][0], sacc[1][1]};
+      float sw[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        sc[k] = (sc[k] - corr) * (ksb[T[k]] * sl);
+        sw[k] = sc[k] + fast_log2(vsb[T[k]]);
+      }
+      if (tok0 + kBS > t_end) {  // slots past the context may hold anything (NaN scales too)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (tok0 + T[k] >= t_end) sc[k] = sw[k] = -INFINITY;
+      }
+      float bm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+      float bw = fmaxf(fmaxf(sw[0], sw[1]), fmaxf(sw[2], sw[3]));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+      bw = fmaxf(bw, __shfl_xor_sync(0xffffffffu, bw, 1));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+      bw = fmaxf(bw, __shfl_xor_sync(0xffffffffu, bw, 2));
+      if (bm > m_run + kLazy || (m_run == -INFINITY && bm != -INFINITY)) {
+        l_part *= fast_exp2(m_run - bm);  // 0 when m_run was -inf
+        m_run = bm;
+      }
+      if (bw > w_run + kLazy || (w_run == -INFINITY && bw != -INFINITY)) {
+        const float beta = fast_exp2(w_run - bw);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          o[j][0] *= beta;
+          o[j][1] *= beta;
+        }
+        z[0] *= beta;
+        z[1] *= beta;
+        w_run = bw;
+      }
+      float wt[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        l_part += sc[k] == -INFINITY ? 0.f : fast_exp2(sc[k] - m_run);
+        wt[k] = sw[k] == -INFINITY ? 0.f : fast_exp2(sw[k] - w_run);
+      }
+      // the score fragment is the A fragment of P V: k-slots (2t, 2t+1) are
+      // tokens T[0], T[1]; (2t+8, 2t+9) are T[2], T[3]
+      const uint32_t pa0 = pack_half2(wt[0], wt[1]);
+      const uint32_t pa2 = pack_half2(wt[2], wt[3]);
+
+      // ---- O += W V: n-tile 4 w + e is dim 16 g + 4 w + e of this lane's
+      // column; lane (g, t) holds dims 32 t + j and 32 t + 16 + j of row g
+      uint4 vr[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) vr[k] = lds128(vb + T[k] * kD + ((g ^ (T[k] & 7)) << 4));
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t a = word(vr[0], w), bb = word(vr[1], w), c2 = word(vr[2], w), d2 = word(vr[3], w);
+        const uint32_t ab_lo = prmt(a, bb, 0x5410u), ab_hi = prmt(a, bb, 0x7632u);
+        const uint32_t cd_lo = prmt(c2, d2, 0x5410u), cd_hi = prmt(c2, d2, 0x7632u);
+        mma_f16(o[4 * w + 0], pa0, 0u, pa2, 0u, codes_to_half2(ab_lo), codes_to_half2(cd_lo));
+        mma_f16(o[4 * w + 1], pa0, 0u, pa2, 0u, codes_to_half2(ab_lo >> 8), codes_to_half2(cd_lo >> 8));
+        mma_f16(o[4 * w + 2], pa0, 0u, pa2, 0u, codes_to_half2(ab_hi), codes_to_half2(cd_hi));
+        mma_f16(o[4 * w + 3], pa0, 0u, pa2, 0u, codes_to_half2(ab_hi >> 8), codes_to_half2(cd_hi >> 8));
+      }
+      // the sum of the weights as the MMA rounds them (B = ones)
+      mma_f16(z, pa0, 0u, pa2, 0u, 0x3C003C00u, 0x3C003C00u);
+    }
+    __syncwarp();
+    if (i + kQ8Stages < my_n) {
+      const int nb = __shfl_sync(0xffffffffu, my_blk, i + kQ8Stages);
+      if (lane == 0) issue(i + kQ8Stages, nb);
+      issued = i + kQ8Stages + 1;
+    }
+  }
+  if (!ok) {
+    for (int i = (issued > kQ8Stages ? issued - kQ8Stages : 0); i < issued; ++i)
+      drain_wait(&wbar[i % kQ8Stages], (i / kQ8Stages) & 1);
+  }
+
+  // ---- warp record per head: o (scaled to m_run), m_run, l
+  l_part += __shfl_xor_sync(0xffffffffu, l_part, 1);
+  l_part += __shfl_xor_sync(0xffffffffu, l_part, 2);
+  constexpr int kRec = kD + 2;
+  if (g < G) {
+    // o = (O - 1152 Z) 2^(w_run - m_run)
+    const float f = (w_run == -INFINITY || m_run == -INFINITY) ? 0.f : fast_exp2(w_run - m_run);
+    const float zb = kBias * z[0];
+    float* rec = comb + (warp * G + g) * kRec;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      rec[32 * t + j] = (o[j][0] - zb) * f;
+      rec[32 * t + 16 + j] = (o[j][1] - zb) * f;
+    }
+    if (t == 0) {
+      rec[kD] = ok ? m_run : -INFINITY;
+      rec[kD + 1] = ok ? l_part : 0.f;
+    }
+  }
+  __syncthreads();
+
+  // ---- combine the warps, write this split's partial (normalised out, log2 LSE)
+  for (int x = threadIdx.x; x < G * kD; x += kWarps * 32) {
+    const int hh = x / kD, d = x % kD;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, comb[(w * G + hh) * kRec + kD]);
+    float lsum = 0.f, osum = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float* rec = comb + (w * G + hh) * kRec;
+        if (rec[kD] == -INFINITY) continue;
+        const float sc = fast_exp2(rec[kD] - M);
+        lsum = fmaf(sc, rec[kD + 1], lsum);
+        osum = fmaf(sc, rec[d], osum);
+      }
+    }
+    const int h = gkv * G + hh;
+    const int64_t slot = (static_cast<int64_t>(b) * p.Hq + h) * p.n_split + split;
+    const bool empty = !(lsum > 0.f);
+    p.o_part[slot * kD + d] = empty ? 0.f : osum / lsum;
+    if (d == 0) p.lse_part[slot] = empty ? -INFINITY : M + __log2f(lsum);
+  }
+}
+
+constexpr size_t q8_mma_smem(int G) {
+  return 1024 + static_cast<size_t>(kWarps) * kQ8Stages * (2 * kCodeBytes + 2 * kBS * 4 + 8) +
+         static_cast<size_t>(kWarps) * G * (kD + 2) * 4;
+}
+
+template <int G>
+cudaError_t launch_g(const DecodeArgs& a, const Q8MmaParams& p, cudaStream_t stream) {
+  auto kern = paged_decode_q8_mma_kernel<G>;
+  const int smem = static_cast<int>(q8_mma_smem(G));
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(static_cast<unsigned>(a.n_split), static_cast<unsigned>(a.cache.Hkv), static_cast<unsigned>(a.B));
+  kern<<<grid, kWarps * 32, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// host side
+
+bool paged_decode_q8_mma_supported(const DecodeArgs& a) {
+  const int64_t G = a.cache.Hkv > 0 ? a.Hq / a.cache.Hkv : 0;
+  return a.cache.k_scale != nullptr && a.cache.D == kD && a.cache.block_size == kBS && a.k_new.data == nullptr &&
+         (G == 1 || G == 2 || G == 4 || G == 8);
+}
+
+cudaError_t launch_paged_decode_q8_mma(const DecodeArgs& a, cudaStream_t stream) {
+  Q8MmaParams p = {};
+  if (!make_code_cache_map(&p.kmap, a.cache.k, a.cache.num_blocks, a.cache.Hkv) ||
+      !make_code_cache_map(&p.vmap, a.cache.v, a.cache.num_blocks, a.cache.Hkv))
+    return cudaErrorInvalidValue;
+  p.ks = a.cache.k_scale;
+  p.vs = a.cache.v_scale;
+  p.num_blocks = a.cache.num_blocks;
+  p.Hkv = a.cache.Hkv;
+  p.Hq = static_cast<int>(a.Hq);
+  p.q = static_cast<const uint16_t*>(a.q.data);
+  p.q_stride[0] = a.q.stride[0];
+  p.q_stride[1] = a.q.stride[1];
+  p.bt = a.block_table;
+  p.bt_stride = a.bt_stride;
+  p.max_blocks = a.max_blocks;
+  p.ctx_lens = a.ctx_lens;
+  p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
+  const size_t n = static_cast<size_t>(a.B) * a.Hq * a.n_split;
+  p.o_part = static_cast<float*>(a.partials);
+  p.lse_part = p.o_part + n * kD;
+  p.n_split = a.n_split;
+  p.status = a.status;
+  cudaError_t e;
+  switch (a.Hq / a.cache.Hkv) {
+    case 1: e = launch_g<1>(a, p, stream); break;
+    case 2: e = launch_g<2>(a, p, stream); break;
+    case 4: e = launch_g<4>(a, p, stream); break;
+    case 8: e = launch_g<8>(a, p, stream); break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
+  return launch_decode_reduce(a, p.o_part, p.lse_part, 0, stream);
+}
+
+}  // namespace attn

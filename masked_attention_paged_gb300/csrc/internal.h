@@ -2,6 +2,7 @@
 // kernel launchers.  Arguments reaching these functions are validated.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -115,6 +116,16 @@ constexpr int kDecodeSplitTokens = 1024;
 int decode_num_splits(int max_blocks, int block_size);
 size_t decode_partial_bytes(int64_t B, int64_t Hq, int n_split, int D);
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);
+// merge the split partials [B, Hq, n_split, D] (+ log2 LSEs) into a.out / a.lse
+cudaError_t launch_decode_reduce(const DecodeArgs& a, const float* o_part, const float* lse_part, int len_add,
+                                 cudaStream_t stream);
+// INT8 cache, D = 128, 16-token blocks, Hq / Hkv in {1, 2, 4, 8}, no fused append:
+// the tensor-core decode (decode_q8.cu) serves the call
+bool paged_decode_q8_mma_supported(const DecodeArgs& a);
+cudaError_t launch_paged_decode_q8_mma(const DecodeArgs& a, cudaStream_t stream);
+// 4-D u8 tensor map over INT8 codes [num_blocks, Hkv, 16, 128] (contiguous):
+// box = the 16 x 128 codes of one (block, head), 128-byte swizzle
+bool make_code_cache_map(CUtensorMap* map, void* base, int64_t num_blocks, int Hkv);
 
 struct PrefillArgs {
   PagedCache cache;

@@ -41,7 +41,7 @@ def _append_decode_check(d, note=""):
     assert_lse_close(lse, rl, what="q8 decode lse" + note)
 
 
-@pytest.mark.parametrize("D,G", [(128, 4), (128, 1), (128, 8), (64, 4), (64, 2)])
+@pytest.mark.parametrize("D,G", [(128, 4), (128, 1), (128, 2), (128, 8), (64, 4), (64, 2)])
 def test_q8_append_and_decode_small(D, G):
     Hkv = 2
     cfg = workloads.DecodeConfig("q", 9, G * Hkv, Hkv, D, 16, 0, 1500, 4)
@@ -106,3 +106,60 @@ def test_q8_decode_tracks_the_bf16_decode():
     out = lib.paged_decode_attn_q8(g["q"], kq, vq, ks, vs, g["block_table"], g["ctx_lens"], d.scale)
     err = (out.float() - ref.float()).abs()
     assert err.max().item() < 3e-2 and err.mean().item() < 3e-3
+
+
+def _decode_only_check(d, scale, note):
+    """Decode the cache as given (no append) with float32 output, against the
+    oracle within a bound taken from the arithmetic: a softmax weight rounded
+    to fp16 is off by at most 2^-11 of itself, so an output element is off by
+    at most 2^-11 sum_t p_t |v_t| / l, which the oracle gives when it decodes
+    |V|; twice that, plus a floor of 1e-6 of the largest such sum."""
+    g = _dev(d)
+    out = torch.empty(d.q.shape, dtype=torch.float32, device=DEV)
+    ws = lib.Workspace(lib.paged_decode_workspace_size(d.cfg.B, d.cfg.Hq, d.block_table.shape[1], 16, d.cfg.D))
+    _, lse = lib.paged_decode_attn_q8(g["q"], g["kq_cache"], g["vq_cache"], g["k_scale"], g["v_scale"],
+                                      g["block_table"], g["ctx"], scale, out=out, return_lse=True, workspace=ws)
+    assert ws.status() == 0
+    kq, vq, ks, vs = d.kq_cache.numpy(), d.vq_cache.numpy(), d.k_scale.numpy(), d.v_scale.numpy()
+    ro, rl = oracle.paged_decode_q8(d.q, kq, vq, ks, vs, d.block_table, d.ctx, scale)
+    ra, _ = oracle.paged_decode_q8(d.q, kq, np.abs(vq), ks, vs, d.block_table, d.ctx, scale)
+    err = np.abs(out.cpu().numpy().astype(np.float64) - ro)
+    bound = 2.0 ** -10 * ra + 1e-6 * ra.max()
+    assert np.all(err <= bound), f"{note}: worst err/bound {(err / bound).max():.3g}"
+    assert_lse_close(lse, rl, what="q8 decode lse " + note)
+
+
+@pytest.mark.parametrize("G", [2, 4])
+def test_q8_decode_wide_scales(G):
+    """Key and value scales spread over 2^-6..2^6 and 2^-13..2^13 of the usual
+    range, some all-zero value rows, and random codes with NaN scales in the
+    unfilled slots: the value scale rides in the softmax weight, so the fp16
+    weights must not lose the small-scale tokens nor overflow on the large."""
+    Hkv = 2
+    cfg = workloads.DecodeConfig("w", 6, G * Hkv, Hkv, 128, 16, 0, 3000, 4)
+    d = workloads.make_decode_inputs_q8(cfg, seed=54, ctx=[1, 17, 700, 1024, 2049, 3000])
+    gen = torch.Generator().manual_seed(55)
+    filled = ~torch.isnan(d.k_scale)
+    d.k_scale[filled] *= torch.exp2(torch.empty(int(filled.sum())).uniform_(-6, 6, generator=gen))
+    d.v_scale[filled] *= torch.exp2(torch.empty(int(filled.sum())).uniform_(-13, 13, generator=gen))
+    zero = filled & (torch.rand(d.v_scale.shape, generator=gen) < 0.05)
+    d.v_scale[zero] = 0.0
+    hole = ~filled
+    junk = torch.randint(-128, 128, d.kq_cache.shape, generator=gen, dtype=torch.int32).to(torch.int8)
+    d.kq_cache[hole] = junk[hole]
+    d.vq_cache[hole] = junk.flip(0)[hole]
+    _decode_only_check(d, d.scale, f"wide scales G={G}")
+
+
+def test_q8_decode_query_beyond_fp16_range():
+    """Query elements up to 1e5 (past fp16's 65504) with a small softmax
+    scale: the tensor-core decode takes q in fp16 after an exact power-of-two
+    prescale, which must leave the result unchanged."""
+    Hkv, G = 2, 4
+    cfg = workloads.DecodeConfig("b", 4, G * Hkv, Hkv, 128, 16, 0, 1200, 4)
+    d = workloads.make_decode_inputs_q8(cfg, seed=56, ctx=[5, 300, 1024, 1200])
+    q = d.q.float()
+    q[:, :, 3] = 1.0e5
+    q[0, 1, 7] = -7.0e4
+    d.q = q.to(torch.bfloat16)
+    _decode_only_check(d, 2.0e-6, "large q")
