@@ -71,13 +71,14 @@ struct Q8MmaParams {
 // bits under the mask take x with the sign bit flipped, the rest the exponent
 __device__ __forceinline__ uint32_t codes_to_half2(uint32_t x) {
   uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(x), "r"(kByteMask), "r"(kHalfBits));
+  asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(d) : "r"(x), "n"(kByteMask), "n"(kHalfBits));
   return d;
 }
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b) {
   uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "n"(SEL));
   return d;
 }
 
@@ -123,7 +124,7 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int w) {
 __device__ __forceinline__ int tok_of(int n) { return n ^ ((n & 1) << 2); }
 
 template <int G>
-__global__ void __launch_bounds__(kWarps * 32, 3) paged_decode_q8_mma_kernel(const __grid_constant__ Q8MmaParams p) {
+__global__ void __launch_bounds__(kWarps * 32, 4) paged_decode_q8_mma_kernel(const __grid_constant__ Q8MmaParams p) {
   static_assert(G >= 1 && G <= 8, "query heads per KV head");
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the swizzled TMA tiles
@@ -131,7 +132,9 @@ __global__ void __launch_bounds__(kWarps * 32, 3) paged_decode_q8_mma_kernel(con
   uint8_t* codes = smem;                                                      // [warp][stage][K, V][2048]
   float* scl = reinterpret_cast<float*>(codes + kWarps * kQ8Stages * 2 * kCodeBytes);  // [warp][stage][K 16, V 16]
   uint64_t* bars = reinterpret_cast<uint64_t*>(scl + kWarps * kQ8Stages * 2 * kBS);
-  float* comb = reinterpret_cast<float*>(bars + kWarps * kQ8Stages);  // [warp][G][D + 2]
+  // [warp][G][D + 2], used once every warp has left its block loop
+  float* comb = reinterpret_cast<float*>(codes);
+  static_assert(kWarps * 8 * (kD + 2) * 4 <= kWarps * kQ8Stages * 2 * kCodeBytes, "combine buffer fits");
 
   const int split = blockIdx.x, gkv = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -171,8 +174,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) paged_decode_q8_mma_kernel(con
       my_blk = -1;
     }
   }
-  auto issue = [&](int i, int blk) {
-    const int s = i % kQ8Stages;
+  auto issue = [&](int s, int blk) {
     if (blk < 0) {  // bad id: complete the phase without data; the block is skipped
       mbar_arrive(&wbar[s]);
       return;
@@ -240,13 +242,18 @@ __global__ void __launch_bounds__(kWarps * 32, 3) paged_decode_q8_mma_kernel(con
   // K fragment rows: token tok_of(g) of each n-tile
   const int krow = tok_of(g);
 
-  float o[16][4];
+  // O^T = V^T W^T: m-tile mt holds dims 16 g + 2 mt (rows g) and 16 g + 2 mt + 1
+  // (rows g + 8) of every head; the columns 2t, 2t+1 are this lane's heads
+  float o[8][4];
 #pragma unroll
-  for (int j = 0; j < 16; ++j)
+  for (int j = 0; j < 8; ++j)
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[j][e] = 0.f;
-  float z[4] = {0.f, 0.f, 0.f, 0.f};
-  float m_run = -INFINITY, w_run = -INFINITY, l_part = 0.f;
+  float z[4] = {0.f, 0.f, 0.f, 0.f};  // per head: the sum of the weights
+  // softmax state of head g: running max (log2), partial sum of p over this
+  // lane's tokens, and the value-weight reference: w = p vs / ref, with ref
+  // shrunk by the same factor as p whenever m_run moves, so O keeps its scale
+  float m_run = -INFINITY, l_part = 0.f, ref = 0.f, ref_inv = 0.f;
 
   __shared__ int abort_flag;
   if (threadIdx.x == 0) abort_flag = 0;
@@ -259,10 +266,11 @@ __global__ void __launch_bounds__(kWarps * 32, 3) paged_decode_q8_mma_kernel(con
     issued = i + 1;
   }
 
+  int s = 0;         // stage of block i
+  uint32_t ph = 0;   // its phase parity
   for (int i = 0; i < my_n; ++i) {
-    const int s = i % kQ8Stages;
     const int blk = __shfl_sync(0xffffffffu, my_blk, i);
-    const bool landed = mbar_wait(&wbar[s], (i / kQ8Stages) & 1, &abort_flag, p.status);
+    const bool landed = mbar_wait(&wbar[s], ph, &abort_flag, p.status);
     if (!__all_sync(0xffffffffu, landed)) {
       ok = false;
       break;
@@ -282,82 +290,108 @@ __global__ void __launch_bounds__(kWarps * 32, 3) paged_decode_q8_mma_kernel(con
         const uint8_t* rowp = kb + tok * kD;
         const uint4 k0 = lds128(rowp + ((t ^ krow) << 4));
         const uint4 k1 = lds128(rowp + (((t + 4) ^ krow) << 4));
+        float s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int e = 0; e < 4; ++e) sacc[j][e] = 0.f;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint32_t x = word(c < 4 ? k0 : k1, c & 3);
-          mma_f16(sacc[j], qa[c][0], 0u, qa[c][1], 0u, codes_to_half2(x), codes_to_half2(x >> 8));
+          mma_f16((c & 1) ? s2 : sacc[j], qa[c][0], 0u, qa[c][1], 0u, codes_to_half2(x), codes_to_half2(x >> 8));
         }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[j][e] += s2[e];
       }
       // scores in log2 units; the key scale multiplies the dot product with the codes
       float sc[4] = {sacc[0][0], sacc[0][1], sacc[1][0], sacc[1][1]};
-      float sw[4];
+      float vsc[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         sc[k] = (sc[k] - corr) * (ksb[T[k]] * sl);
-        sw[k] = sc[k] + fast_log2(vsb[T[k]]);
+        vsc[k] = vsb[T[k]];
       }
       if (tok0 + kBS > t_end) {  // slots past the context may hold anything (NaN scales too)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          if (tok0 + T[k] >= t_end) sc[k] = sw[k] = -INFINITY;
+          if (tok0 + T[k] >= t_end) {
+            sc[k] = -INFINITY;
+            vsc[k] = 0.f;
+          }
       }
       float bm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-      float bw = fmaxf(fmaxf(sw[0], sw[1]), fmaxf(sw[2], sw[3]));
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
-      bw = fmaxf(bw, __shfl_xor_sync(0xffffffffu, bw, 1));
       bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-      bw = fmaxf(bw, __shfl_xor_sync(0xffffffffu, bw, 2));
-      if (bm > m_run + kLazy || (m_run == -INFINITY && bm != -INFINITY)) {
-        l_part *= fast_exp2(m_run - bm);  // 0 when m_run was -inf
+      if (bm > m_run + kLazy) {  // lazy: the reference max moves only by more than the margin
+        const float alpha = fast_exp2(m_run - bm);  // 0 when m_run was -inf
+        l_part *= alpha;
+        // a reference shrunk to nothing is dropped (the next block sets a new
+        // one); the weights it carried are below 1e-30 of any later block's
+        ref *= alpha;
+        if (!(ref > 1e-30f)) ref = 0.f;
+        ref_inv = ref > 0.f ? 1.f / ref : 0.f;
         m_run = bm;
       }
-      if (bw > w_run + kLazy || (w_run == -INFINITY && bw != -INFINITY)) {
-        const float beta = fast_exp2(w_run - bw);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          o[j][0] *= beta;
-          o[j][1] *= beta;
-        }
-        z[0] *= beta;
-        z[1] *= beta;
-        w_run = bw;
-      }
-      float wt[4];
+      float pr[4], u[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        l_part += sc[k] == -INFINITY ? 0.f : fast_exp2(sc[k] - m_run);
-        wt[k] = sw[k] == -INFINITY ? 0.f : fast_exp2(sw[k] - w_run);
+        pr[k] = fast_exp2(sc[k] - m_run);
+        u[k] = pr[k] * vsc[k];
       }
-      // the score fragment is the A fragment of P V: k-slots (2t, 2t+1) are
-      // tokens T[0], T[1]; (2t+8, 2t+9) are T[2], T[3]
-      const uint32_t pa0 = pack_half2(wt[0], wt[1]);
-      const uint32_t pa2 = pack_half2(wt[2], wt[3]);
+      l_part += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+      float um = fmaxf(fmaxf(u[0], u[1]), fmaxf(u[2], u[3]));
+      um = fmaxf(um, __shfl_xor_sync(0xffffffffu, um, 1));
+      um = fmaxf(um, __shfl_xor_sync(0xffffffffu, um, 2));
+      // keep w = u / ref in [0, 2^8]: a larger block moves the reference and
+      // rescales the output columns of its head (held by the lanes t = h / 2)
+      const bool grow = um > ref * 256.f;
+      if (__any_sync(0xffffffffu, grow)) {
+        const float gam = grow ? ref / um : 1.f;
+        if (grow) {
+          ref = um;
+          ref_inv = 1.f / um;
+        }
+        const float f0 = __shfl_sync(0xffffffffu, gam, 8 * t), f1 = __shfl_sync(0xffffffffu, gam, 8 * t + 4);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          o[j][0] *= f0;
+          o[j][1] *= f1;
+          o[j][2] *= f0;
+          o[j][3] *= f1;
+        }
+        z[0] *= f0;
+        z[1] *= f1;
+      }
+      // the weights of head g are the B fragment of O^T = V^T W^T: k-slots
+      // (2t, 2t+1) are tokens T[0], T[1]; (2t+8, 2t+9) are T[2], T[3]
+      const uint32_t pb0 = pack_half2(u[0] * ref_inv, u[1] * ref_inv);
+      const uint32_t pb1 = pack_half2(u[2] * ref_inv, u[3] * ref_inv);
 
-      // ---- O += W V: n-tile 4 w + e is dim 16 g + 4 w + e of this lane's
-      // column; lane (g, t) holds dims 32 t + j and 32 t + 16 + j of row g
+      // ---- O^T += V^T W^T over the lane's 16-dim chunk g of tokens T[0..3]
       uint4 vr[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) vr[k] = lds128(vb + T[k] * kD + ((g ^ (T[k] & 7)) << 4));
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         const uint32_t a = word(vr[0], w), bb = word(vr[1], w), c2 = word(vr[2], w), d2 = word(vr[3], w);
-        const uint32_t ab_lo = prmt(a, bb, 0x5410u), ab_hi = prmt(a, bb, 0x7632u);
-        const uint32_t cd_lo = prmt(c2, d2, 0x5410u), cd_hi = prmt(c2, d2, 0x7632u);
-        mma_f16(o[4 * w + 0], pa0, 0u, pa2, 0u, codes_to_half2(ab_lo), codes_to_half2(cd_lo));
-        mma_f16(o[4 * w + 1], pa0, 0u, pa2, 0u, codes_to_half2(ab_lo >> 8), codes_to_half2(cd_lo >> 8));
-        mma_f16(o[4 * w + 2], pa0, 0u, pa2, 0u, codes_to_half2(ab_hi), codes_to_half2(cd_hi));
-        mma_f16(o[4 * w + 3], pa0, 0u, pa2, 0u, codes_to_half2(ab_hi >> 8), codes_to_half2(cd_hi >> 8));
+        const uint32_t ab_lo = prmt<0x5410u>(a, bb), ab_hi = prmt<0x7632u>(a, bb);
+        const uint32_t cd_lo = prmt<0x5410u>(c2, d2), cd_hi = prmt<0x7632u>(c2, d2);
+        // m-tile 2w: bytes 4w (rows g), 4w + 1 (rows g + 8); m-tile 2w + 1: bytes 4w + 2, 4w + 3
+        mma_f16(o[2 * w], codes_to_half2(ab_lo), codes_to_half2(ab_lo >> 8), codes_to_half2(cd_lo),
+                codes_to_half2(cd_lo >> 8), pb0, pb1);
+        mma_f16(o[2 * w + 1], codes_to_half2(ab_hi), codes_to_half2(ab_hi >> 8), codes_to_half2(cd_hi),
+                codes_to_half2(cd_hi >> 8), pb0, pb1);
       }
-      // the sum of the weights as the MMA rounds them (B = ones)
-      mma_f16(z, pa0, 0u, pa2, 0u, 0x3C003C00u, 0x3C003C00u);
+      // the sum of the weights as the MMA rounds them (A = ones)
+      mma_f16(z, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, pb0, pb1);
     }
     __syncwarp();
     if (i + kQ8Stages < my_n) {
       const int nb = __shfl_sync(0xffffffffu, my_blk, i + kQ8Stages);
-      if (lane == 0) issue(i + kQ8Stages, nb);
+      if (lane == 0) issue(s, nb);  // block i + kQ8Stages reuses stage s
       issued = i + kQ8Stages + 1;
+    }
+    if (++s == kQ8Stages) {
+      s = 0;
+      ph ^= 1u;
     }
   }
   if (!ok) {
@@ -368,20 +402,26 @@ __global__ void __launch_bounds__(kWarps * 32, 3) paged_decode_q8_mma_kernel(con
   // ---- warp record per head: o (scaled to m_run), m_run, l
   l_part += __shfl_xor_sync(0xffffffffu, l_part, 1);
   l_part += __shfl_xor_sync(0xffffffffu, l_part, 2);
+  __syncthreads();  // the records overwrite the code buffers
   constexpr int kRec = kD + 2;
-  if (g < G) {
-    // o = (O - 1152 Z) 2^(w_run - m_run)
-    const float f = (w_run == -INFINITY || m_run == -INFINITY) ? 0.f : fast_exp2(w_run - m_run);
-    const float zb = kBias * z[0];
+  if (g < G && t == 0) {
     float* rec = comb + (warp * G + g) * kRec;
+    rec[kD] = (ok && m_run != -INFINITY) ? m_run : -INFINITY;
+    rec[kD + 1] = ok ? l_part : 0.f;
+  }
+  // columns 2t, 2t+1: o = (O - 1152 Z) ref of that head (ref from lane 4 h)
+  const float r0 = __shfl_sync(0xffffffffu, ref, 8 * t), r1 = __shfl_sync(0xffffffffu, ref, 8 * t + 4);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      rec[32 * t + j] = (o[j][0] - zb) * f;
-      rec[32 * t + 16 + j] = (o[j][1] - zb) * f;
-    }
-    if (t == 0) {
-      rec[kD] = ok ? m_run : -INFINITY;
-      rec[kD + 1] = ok ? l_part : 0.f;
+  for (int hc = 0; hc < 2; ++hc) {
+    const int h = 2 * t + hc;
+    if (h < G) {
+      const float zb = kBias * z[hc], rr = hc ? r1 : r0;
+      float* rec = comb + (warp * G + h) * kRec + 16 * g;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        rec[2 * j] = (o[j][hc] - zb) * rr;
+        rec[2 * j + 1] = (o[j][2 + hc] - zb) * rr;
+      }
     }
   }
   __syncthreads();
@@ -411,15 +451,14 @@ __global__ void __launch_bounds__(kWarps * 32, 3) paged_decode_q8_mma_kernel(con
   }
 }
 
-constexpr size_t q8_mma_smem(int G) {
-  return 1024 + static_cast<size_t>(kWarps) * kQ8Stages * (2 * kCodeBytes + 2 * kBS * 4 + 8) +
-         static_cast<size_t>(kWarps) * G * (kD + 2) * 4;
+constexpr size_t q8_mma_smem() {
+  return 1024 + static_cast<size_t>(kWarps) * kQ8Stages * (2 * kCodeBytes + 2 * kBS * 4 + 8);
 }
 
 template <int G>
 cudaError_t launch_g(const DecodeArgs& a, const Q8MmaParams& p, cudaStream_t stream) {
   auto kern = paged_decode_q8_mma_kernel<G>;
-  const int smem = static_cast<int>(q8_mma_smem(G));
+  const int smem = static_cast<int>(q8_mma_smem());
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(a.n_split), static_cast<unsigned>(a.cache.Hkv), static_cast<unsigned>(a.B));
