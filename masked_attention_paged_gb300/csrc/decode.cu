@@ -432,13 +432,17 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeP
 }
 
 // Merge the splits of each (sequence, head): the LSE rule of the ring-attention
-// page, with the LSEs in log2 units.  One warp per (sequence, head).
+// page, with the LSEs in log2 units.  One warp per (sequence, head): lane s
+// holds split s's LSE (32 splits per pass), the warp max and the weights come
+// from shuffles, and the partial outputs of up to 8 splits are loaded before
+// any is used, so the merge costs a few memory latencies, not one per split.
 template <int D>
 __global__ void decode_reduce_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                                      const int32_t* __restrict__ ctx_lens, int len_add, int max_tokens, int n_split,
                                      int64_t B, int Hq, void* out, int out_bf16, int64_t os0, int64_t os1,
                                      float* lse) {
   constexpr int DPL = D / 32;  // dims per lane
+  constexpr int kBatch = 8;    // splits whose outputs are in flight together
   const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= B * Hq) return;
@@ -448,22 +452,42 @@ __global__ void decode_reduce_kernel(const float* __restrict__ o_part, const flo
   L = L < 0 ? 0 : (L > max_tokens ? max_tokens : L);
   const int ns = (L + kDecodeSplitTokens - 1) / kDecodeSplitTokens;
   const int64_t base = wid * n_split;
-  float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) M = fmaxf(M, lse_part[base + s]);
+  const float ls0 = lane < ns ? lse_part[base + lane] : -INFINITY;
+  float M = ls0;
+  for (int s0 = 32; s0 < ns; s0 += 32)
+    if (s0 + lane < ns) M = fmaxf(M, lse_part[base + s0 + lane]);
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
   float acc[DPL];
 #pragma unroll
   for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
   float wsum = 0.f;
   if (M != -INFINITY) {
-    for (int s = 0; s < ns; ++s) {
-      const float ls = lse_part[base + s];
-      if (ls == -INFINITY) continue;
-      const float w = fast_exp2(ls - M);
+    for (int s0 = 0; s0 < ns; s0 += 32) {
+      const float ls = s0 == 0 ? ls0 : (s0 + lane < ns ? lse_part[base + s0 + lane] : -INFINITY);
+      const float w = ls == -INFINITY ? 0.f : fast_exp2(ls - M);
       wsum += w;
-      const float* op = o_part + (base + s) * D + lane * DPL;
+      const int n = min(32, ns - s0);
+      for (int k0 = 0; k0 < n; k0 += kBatch) {
+        float ov[kBatch][DPL];
+        float wk[kBatch];
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) acc[e] = fmaf(w, op[e], acc[e]);
+        for (int u = 0; u < kBatch; ++u) {
+          wk[u] = __shfl_sync(0xffffffffu, w, (k0 + u) & 31);
+          const bool use = k0 + u < n && wk[u] > 0.f;  // empty splits may hold anything
+          const float* op = o_part + (base + s0 + k0 + u) * D + lane * DPL;
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) ov[u][e] = use ? op[e] : 0.f;
+          if (!use) wk[u] = 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wk[u], ov[u][e], acc[e]);
+      }
     }
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, m);
   }
   const bool empty = !(wsum > 0.f);
   const float inv = empty ? 0.f : 1.f / wsum;

@@ -15,12 +15,15 @@
 //    sum of the weights, which a further MMA against a tile of ones yields in
 //    the same rounding as the output;
 //  * scores S = Q K^T with the query heads as the A rows (zero padded) and
-//    the 16 tokens of a block as two n-tiles; the score fragment is, register
-//    for register, the A fragment of the P V product, so no shuffle moves it;
-//  * the key scale multiplies the score; the value scale joins the softmax
-//    weight through a second exponent stream, w = 2^(s + log2 vs - M) with its
-//    own running max M, so the fp16 weights stay in [0, 2^8] whatever the
-//    scales are, and O accumulates straight in the MMA registers;
+//    the 16 tokens of a block as two n-tiles; the values go in transposed,
+//    O^T = V^T W^T, where the weight fragment of a head is, register for
+//    register, its score fragment: no shuffle moves it, and the output tile
+//    is 128 dims x 8 heads;
+//  * the key scale multiplies the score; the value scale multiplies the
+//    softmax weight, w = p vs / ref, against a per-head reference that moves
+//    lazily (up with the largest p vs of a block, down with the running max),
+//    so the fp16 weights stay in [0, 2^8] whatever the scales are and O
+//    accumulates straight in the MMA registers;
 //  * each warp streams its blocks with two 4-D TMA loads per block (K and V
 //    codes, 128-byte swizzle) plus two bulk copies of the row scales; tokens
 //    are taken in the order n ^ ((n & 1) << 2) within each group of eight,
@@ -96,12 +99,6 @@ __device__ __forceinline__ float half2_sum(uint32_t x) {
       : "=f"(lo), "=f"(hi)
       : "r"(x));
   return lo + hi;
-}
-
-__device__ __forceinline__ float fast_log2(float x) {
-  float y;
-  asm("lg2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
 }
 
 // D (16x8, fp32) += A (16x16, fp16, rows g and g+8 in a0/a2 and a1/a3) * B (16x8)

@@ -36,7 +36,8 @@ def assert_lse_close(gpu, ref, what="lse"):
     assert g.shape == r.shape, (g.shape, r.shape)
     both_inf = np.isneginf(g) & np.isneginf(r)
     assert np.array_equal(np.isneginf(g), np.isneginf(r)), f"{what}: -inf pattern differs"
-    err = np.abs(np.where(both_inf, 0.0, g - r))
+    with np.errstate(invalid="ignore"):  # -inf - -inf where both are -inf, masked out
+        err = np.abs(np.where(both_inf, 0.0, g - r))
     assert err.max() <= LSE_ABS, f"{what}: max abs err {err.max():.3g} > {LSE_ABS}"
     return err.max()
 

@@ -111,6 +111,14 @@ def test_paged_decode_small(D, G):
     _decode_and_check(d, f" D={D} G={G}")
 
 
+def test_paged_decode_long_context():
+    """Contexts of 40,000 and 33,000 tokens: 40 and 33 splits of 1024, more
+    than the 32 the split merge takes in one pass."""
+    cfg = workloads.DecodeConfig("l", 3, 8, 2, 128, 16, 0, 40000, 4)
+    d = workloads.make_decode_inputs(cfg, seed=19, ctx=[40000, 33000, 100])
+    _decode_and_check(d, " long")
+
+
 def test_paged_decode_f32_output_and_strided_q():
     cfg = workloads.DecodeConfig("s", 3, 8, 2, 128, 16, 100, 600, 2)
     d = workloads.make_decode_inputs(cfg, seed=8)

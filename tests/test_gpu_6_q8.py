@@ -49,6 +49,13 @@ def test_q8_append_and_decode_small(D, G):
     _append_decode_check(d, f" D={D} G={G}")
 
 
+def test_q8_long_context():
+    """40 and 33 splits of 1024 tokens: the split merge's second pass."""
+    cfg = workloads.DecodeConfig("l", 3, 8, 2, 128, 16, 0, 40000, 4)
+    d = workloads.make_decode_inputs_q8(cfg, seed=57, ctx=[40000, 33000, 100])
+    _append_decode_check(d, " long")
+
+
 def test_q8_full_decode_workload():
     d = workloads.make_decode_inputs_q8(workloads.DECODE_CONFIGS["decode"], seed=0)
     _append_decode_check(d, " full")
