@@ -292,71 +292,76 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(smem + C::kOffQ + t * C::kTileBytes + x * kBoxBytes, &tm_q, &bars->q_full, x * 64, c1, c2,
                       c3);
       }
-      int k_issued = 0, v_issued = 0;
+    }
+    int k_issued = 0, v_issued = 0;
+    if constexpr (PAGED) {
+      // the whole warp streams K/V: lane i < 8 owns logical block 8j + i of
+      // key tile j (its two 64-column boxes of K and of V), so one
+      // warp-instruction issues a half of every block; the ids are read one
+      // tile ahead.  Blocks wholly past the CTA's last key are not loaded,
+      // nor is a bad block id.
+      constexpr int kBlk = kBN / 16;
+      constexpr int kBlockBytes = 16 * D * 2;
+      const int32_t* bt_row = prm.bt + static_cast<int64_t>(b) * prm.bt_stride + kv0 * kBlk;
+      auto block_id = [&](int j) {
+        const int nb = min(kBlk, (n_keys - (kv0 + j) * kBN + 15) / 16);
+        return (j < nkv && lane < nb) ? bt_row[j * kBlk + lane] : -1;
+      };
+      int id_next = block_id(0);
       for (int j = 0; j < nkv; ++j) {
         const int s = j % C::kStages;
         const uint32_t ph = (j / C::kStages) & 1;
-        if constexpr (PAGED) {
-          // the tile's keys sit in logical blocks 8j .. 8j+7; blocks wholly
-          // past the CTA's last key are not loaded, nor is a bad block id
-          constexpr int kBlk = kBN / 16;
-          const int nb = min(kBlk, (n_keys - (kv0 + j) * kBN + 15) / 16);
-          const int32_t* row = prm.bt + static_cast<int64_t>(b) * prm.bt_stride + (kv0 + j) * kBlk;
-          int ids[kBlk];
-          int n_ok = 0;
-#pragma unroll
-          for (int i = 0; i < kBlk; ++i) {
-            ids[i] = -1;
-            if (i < nb) {
-              const int id = row[i];
-              if (id < 0 || id >= prm.num_blocks) {
-                report(prm.status, kStatusBounds);
-              } else {
-                ids[i] = id;
-                ++n_ok;
-              }
-            }
-          }
-          constexpr int kBlockBytes = 16 * D * 2;
-          if (!mbar_wait(&bars->k_empty[s], ph ^ 1, abort, prm.status)) break;
-          mbar_arrive_expect_tx(&bars->k_full[s], n_ok * kBlockBytes);
-#pragma unroll
-          for (int i = 0; i < kBlk; ++i)
-            if (ids[i] >= 0)
-#pragma unroll
-              for (int x = 0; x < C::kBoxes; ++x)
-                tma_load_4d(smem + C::kOffK + s * C::kTileBytes + x * kBoxBytes + i * 2048, &tm_k, &bars->k_full[s],
-                            x * 64, 0, g, ids[i]);
-          k_issued = j + 1;
-          if (!mbar_wait(&bars->v_empty[s], ph ^ 1, abort, prm.status)) break;
-          mbar_arrive_expect_tx(&bars->v_full[s], n_ok * kBlockBytes);
-#pragma unroll
-          for (int i = 0; i < kBlk; ++i)
-            if (ids[i] >= 0)
-#pragma unroll
-              for (int x = 0; x < C::kBoxes; ++x)
-                tma_load_4d(smem + C::kOffV + s * C::kTileBytes + x * kBoxBytes + i * 2048, &tm_v, &bars->v_full[s],
-                            x * 64, 0, g, ids[i]);
-          v_issued = j + 1;
-        } else {
-          if (!mbar_wait(&bars->k_empty[s], ph ^ 1, abort, prm.status)) break;
-          mbar_arrive_expect_tx(&bars->k_full[s], C::kTileBytes);
-          coords(prm.ck, (kv0 + j) * kBN, g, b, c1, c2, c3);
-#pragma unroll
-          for (int x = 0; x < C::kBoxes; ++x)
-            tma_load_4d(smem + C::kOffK + s * C::kTileBytes + x * kBoxBytes, &tm_k, &bars->k_full[s], x * 64,
-                        c1, c2, c3);
-          k_issued = j + 1;
-          if (!mbar_wait(&bars->v_empty[s], ph ^ 1, abort, prm.status)) break;
-          mbar_arrive_expect_tx(&bars->v_full[s], C::kTileBytes);
-          coords(prm.cv, (kv0 + j) * kBN, g, b, c1, c2, c3);
-#pragma unroll
-          for (int x = 0; x < C::kBoxes; ++x)
-            tma_load_4d(smem + C::kOffV + s * C::kTileBytes + x * kBoxBytes, &tm_v, &bars->v_full[s], x * 64,
-                        c1, c2, c3);
-          v_issued = j + 1;
+        int id = id_next;
+        id_next = block_id(j + 1);
+        if (lane < kBlk && id != -1 && (id < 0 || id >= prm.num_blocks)) {
+          report(prm.status, kStatusBounds);
+          id = -1;
         }
+        if (id >= 0 && lane >= kBlk) id = -1;
+        const int n_ok = __popc(__ballot_sync(0xffffffffu, id >= 0));
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->k_empty[s], ph ^ 1, abort, prm.status))) break;
+        if (lane == 0) mbar_arrive_expect_tx(&bars->k_full[s], n_ok * kBlockBytes);
+        __syncwarp();
+        if (id >= 0)
+#pragma unroll
+          for (int x = 0; x < C::kBoxes; ++x)
+            tma_load_4d(smem + C::kOffK + s * C::kTileBytes + x * kBoxBytes + lane * 2048, &tm_k, &bars->k_full[s],
+                        x * 64, 0, g, id);
+        k_issued = j + 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bars->v_empty[s], ph ^ 1, abort, prm.status))) break;
+        if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[s], n_ok * kBlockBytes);
+        __syncwarp();
+        if (id >= 0)
+#pragma unroll
+          for (int x = 0; x < C::kBoxes; ++x)
+            tma_load_4d(smem + C::kOffV + s * C::kTileBytes + x * kBoxBytes + lane * 2048, &tm_v, &bars->v_full[s],
+                        x * 64, 0, g, id);
+        v_issued = j + 1;
       }
+    } else if (lane == 0) {
+      int c1, c2, c3;
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % C::kStages;
+        const uint32_t ph = (j / C::kStages) & 1;
+        if (!mbar_wait(&bars->k_empty[s], ph ^ 1, abort, prm.status)) break;
+        mbar_arrive_expect_tx(&bars->k_full[s], C::kTileBytes);
+        coords(prm.ck, (kv0 + j) * kBN, g, b, c1, c2, c3);
+#pragma unroll
+        for (int x = 0; x < C::kBoxes; ++x)
+          tma_load_4d(smem + C::kOffK + s * C::kTileBytes + x * kBoxBytes, &tm_k, &bars->k_full[s], x * 64,
+                      c1, c2, c3);
+        k_issued = j + 1;
+        if (!mbar_wait(&bars->v_empty[s], ph ^ 1, abort, prm.status)) break;
+        mbar_arrive_expect_tx(&bars->v_full[s], C::kTileBytes);
+        coords(prm.cv, (kv0 + j) * kBN, g, b, c1, c2, c3);
+#pragma unroll
+        for (int x = 0; x < C::kBoxes; ++x)
+          tma_load_4d(smem + C::kOffV + s * C::kTileBytes + x * kBoxBytes, &tm_v, &bars->v_full[s], x * 64,
+                      c1, c2, c3);
+        v_issued = j + 1;
+      }
+    }
+    if (lane == 0) {
       if (*abort) {
         // let every copy still in flight land before the CTA exits
         drain_wait(&bars->q_full, 0);
