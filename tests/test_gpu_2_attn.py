@@ -187,7 +187,8 @@ def test_patch_large_workload_sampled():
     assert_lse_close(l.reshape(-1)[torch.from_numpy(rows).to(DEV)], rl)
 
 
-@pytest.mark.parametrize("dtype,n", [(torch.bfloat16, 2), (torch.float32, 3), (torch.bfloat16, 5)])
+@pytest.mark.parametrize("dtype,n", [(torch.bfloat16, 2), (torch.float32, 2), (torch.float32, 3), (torch.bfloat16, 4),
+                                     (torch.bfloat16, 5)])
 def test_lse_merge_against_oracle(dtype, n):
     """Chunk partials from the oracle, merged on the GPU, against the oracle's
     merge; one chunk holds only padded keys so its lse is -inf."""
