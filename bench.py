@@ -465,7 +465,7 @@ def next_rows(step, K, W, pk):
                                  "ms": q_ms, "gbs": q8_bytes / (q_ms * 1e-3) / 1e9,
                                  "frac": q8_bytes / (q_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
                                  "speedup_vs_bf16_decode": (step.decode_ms_ref / q_ms) if step.decode_ms_ref else None,
-                                 "launches": 3, "bytes": q8_bytes, "traffic": traffic("paged_decode_kernel_q8")},
+                                 "launches": 3, "bytes": q8_bytes, "traffic": traffic("paged_decode_q8_mma_kernel")},
         "paged_prefill_attn": {"workload": "prefill_chunk (16 seqs x 1024-token causal chunk after U[0, 7168] "
                                            "cached, Hq 32, Hkv 8, D 128)",
                                "ms": p_ms, "tflops": p_tf, "frac": p_tf / peak_t, "launches": 2,
