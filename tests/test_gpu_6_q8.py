@@ -170,3 +170,29 @@ def test_q8_decode_query_beyond_fp16_range():
     q[0, 1, 7] = -7.0e4
     d.q = q.to(torch.bfloat16)
     _decode_only_check(d, 2.0e-6, "large q")
+
+
+def test_q8_decode_empty_context_and_bad_block():
+    """An empty context gives out = 0 and lse = -inf; a table entry outside
+    the cache is reported (status 5) and skipped without a fault."""
+    cfg = workloads.DecodeConfig("e", 3, 8, 2, 128, 16, 0, 200, 2)
+    d = workloads.make_decode_inputs_q8(cfg, seed=58, ctx=[10, 100, 200])
+    g = _dev(d)
+    lens = g["ctx"].clone()
+    lens[0] = 0
+    ws = lib.Workspace(lib.paged_decode_workspace_size(3, 8, d.block_table.shape[1], 16, 128))
+    out, lse = lib.paged_decode_attn_q8(g["q"], g["kq_cache"], g["vq_cache"], g["k_scale"], g["v_scale"],
+                                        g["block_table"], lens, d.scale, return_lse=True, workspace=ws)
+    assert ws.status() == 0
+    assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
+    lens_cpu = lens.cpu()
+    ro, rl = oracle.paged_decode_q8(d.q[1:], d.kq_cache.numpy(), d.vq_cache.numpy(), d.k_scale.numpy(),
+                                    d.v_scale.numpy(), d.block_table[1:], lens_cpu[1:], d.scale)
+    assert_out_close(out[1:], ro)
+    assert_lse_close(lse[1:], rl)
+    bt = g["block_table"].clone()
+    bt[2, 3] = -7
+    ws.reset()
+    lib.paged_decode_attn_q8(g["q"], g["kq_cache"], g["vq_cache"], g["k_scale"], g["v_scale"], bt, lens, d.scale,
+                             workspace=ws)
+    assert ws.status() == 5
