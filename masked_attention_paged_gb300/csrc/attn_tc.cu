@@ -573,14 +573,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       uint32_t sr[4][32];
+      // D = 128: the first half of the scores first; the second half is
+      // loaded while the fast path exponentiates the first
+      constexpr int kFirstLd = C::kSepP ? 4 : 2;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_addr + s_col + c * 32, sr[c]);
+      for (int c = 0; c < kFirstLd; ++c) tmem_ld32(tmem + lane_addr + s_col + c * 32, sr[c]);
       // keys of this tile the row may see: [0, lim)
       const int lim = row_lim - (kv0 + j) * kBN;
       const bool masked_tile = PAGED ? __any_sync(0xffffffffu, lim < kBN) || !prm.scale_positive
                                      : bars->m_flag[mb_i] != 0;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
+      for (int c = 0; c < kFirstLd; ++c) tmem_wait_ld(sr[c]);
+#pragma unroll
+      for (int c = kFirstLd; c < 4; ++c) tmem_ld32(tmem + lane_addr + s_col + c * 32, sr[c]);
+      bool second_pending = kFirstLd < 4;
+      auto finish_ld = [&]() {
+        if (second_pending) {
+#pragma unroll
+          for (int c = kFirstLd; c < 4; ++c) tmem_wait_ld(sr[c]);
+          second_pending = false;
+        }
+      };
 #define SV(c) __uint_as_float(sr[(c) >> 5][(c) & 31])
       if constexpr (C::kSepP) {  // S is in registers: the next S may overwrite it
         tc_fence_before();
@@ -615,6 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // two keys per packed fma / add; sums in 8 partial accumulators
 #pragma unroll
         for (int c = 0; c < kBN; c += 2) {
+          if (c == kFirstLd * 32) finish_ld();
           float x0, x1;
           f2_unpack(ffma2(f2_pack(SV(c), SV(c + 1)), sc2, ng2), x0, x1);
           const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
@@ -635,6 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!done) {
+        finish_ld();
         // tile max in log2 units: 8 independent chains of 3-input max
         float mx[8];
         if (!masked_tile) {
@@ -870,12 +885,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Merge the KV parts of each split unit: per query row, the LSE rule of the
 // ring-attention page (out = sum_c exp(lse_c - lse) out_c) over its `split`
-// normalised partials.  One warp per row.
+// (<= 8) normalised partials.  One warp per row: lane c holds part c's LSE,
+// the max and the weights come from shuffles, and every part's row is
+// loaded before any is used.
 template <int D, bool OUT_BF16>
 __global__ void split_merge_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse, int split,
                                    int full_units, int tail, int nq, int Hq, int Pq, void* out, int64_t os0,
                                    int64_t os1, int64_t os2, float* lse) {
   constexpr int E = D / 32;
+  constexpr int kMaxParts = 8;
   const int w = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (w >= tail * 2 * kBM) return;
@@ -884,21 +902,34 @@ __global__ void split_merge_kernel(const float* __restrict__ part_o, const float
   const int qi = (unit % nq) * (2 * kBM) + r;
   if (qi >= Pq) return;
   const int h = (unit / nq) % Hq, b = unit / (nq * Hq);
-  float M = -INFINITY;
-  for (int c = 0; c < split; ++c) M = fmaxf(M, part_lse[static_cast<int64_t>(u * split + c) * (2 * kBM) + r]);
+  const float l_mine =
+      lane < split ? part_lse[static_cast<int64_t>(u * split + lane) * (2 * kBM) + r] : -INFINITY;
+  float M = l_mine;
+#pragma unroll
+  for (int m = 4; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
+  M = __shfl_sync(0xffffffffu, M, 0);  // lanes 0-7 hold the parts
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.0f;
   float wsum = 0.0f;
   if (M != -INFINITY) {
-    for (int c = 0; c < split; ++c) {
-      const int64_t prow = static_cast<int64_t>(u * split + c) * (2 * kBM) + r;
-      const float l = part_lse[prow];
-      if (l == -INFINITY) continue;
-      const float wt = expf(l - M);
-      wsum += wt;
+    const float w_mine = l_mine == -INFINITY ? 0.0f : expf(l_mine - M);
+    float ov[kMaxParts][E];
+    float wk[kMaxParts];
 #pragma unroll
-      for (int e = 0; e < E; ++e) acc[e] = fmaf(wt, part_o[prow * D + lane * E + e], acc[e]);
+    for (int c = 0; c < kMaxParts; ++c) {
+      wk[c] = __shfl_sync(0xffffffffu, w_mine, c);
+      const bool use = c < split && wk[c] > 0.0f;  // a part with no keys may hold anything
+      const int64_t prow = static_cast<int64_t>(u * split + c) * (2 * kBM) + r;
+#pragma unroll
+      for (int e = 0; e < E; ++e) ov[c][e] = use ? part_o[prow * D + lane * E + e] : 0.0f;
+      if (!use) wk[c] = 0.0f;
+    }
+#pragma unroll
+    for (int c = 0; c < kMaxParts; ++c) {
+      wsum += wk[c];
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(wk[c], ov[c][e], acc[e]);
     }
   }
   const bool empty = !(wsum > 0.0f);
