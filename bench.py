@@ -604,8 +604,8 @@ def main():
                      "traffic": traffic("attn_fwd_tc_kernel"),
                      "peak_source": f"{pk['source']} bf16 sustained (kernel timed inside a long step)",
                      "work_per_launch": "4*T*Pk*H*D = 6.594 TFLOP (T 32760, Pk 16380, H 24, D 128)"},
-        "decode": {"bound": "hbm", "kernel": "paged_decode_kernel", "achieved": dec_gbs, "peak": pk["hbm_gbs"],
-                   "unit": "GB/s", "frac": dec_gbs / pk["hbm_gbs"], "traffic": traffic("paged_decode_kernel"),
+        "decode": {"bound": "hbm", "kernel": "paged_decode_tc_kernel", "achieved": dec_gbs, "peak": pk["hbm_gbs"],
+                   "unit": "GB/s", "frac": dec_gbs / pk["hbm_gbs"], "traffic": traffic("paged_decode_tc_kernel"),
                    "work_per_launch": f"{step.decode_bytes} B (K/V of every attended token, q, out, table)"},
         "rows": rows,
         "clocks": clk,

@@ -1034,6 +1034,10 @@ bool make_cache_map(CUtensorMap* map, void* base, int64_t num_blocks, int Hkv, i
 
 }  // namespace
 
+bool make_bf16_cache_map(CUtensorMap* map, void* base, int64_t num_blocks, int Hkv) {
+  return make_cache_map(map, base, num_blocks, Hkv, 128);
+}
+
 bool make_code_cache_map(CUtensorMap* map, void* base, int64_t num_blocks, int Hkv) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;

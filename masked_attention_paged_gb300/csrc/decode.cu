@@ -547,6 +547,7 @@ cudaError_t launch_decode_reduce(const DecodeArgs& a, const float* o_part, const
 }
 
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
+  if (paged_decode_tc_supported(a)) return launch_paged_decode_tc(a, stream);
   if (paged_decode_q8_mma_supported(a)) return launch_paged_decode_q8_mma(a, stream);
   DecodeParams p;
   p.kc = a.cache.k;

@@ -126,6 +126,13 @@ cudaError_t launch_paged_decode_q8_mma(const DecodeArgs& a, cudaStream_t stream)
 // 4-D u8 tensor map over INT8 codes [num_blocks, Hkv, 16, 128] (contiguous):
 // box = the 16 x 128 codes of one (block, head), 128-byte swizzle
 bool make_code_cache_map(CUtensorMap* map, void* base, int64_t num_blocks, int Hkv);
+// bf16 cache, D = 128, 16-token blocks, Hq / Hkv in {1, 2, 4, 8}: the tensor-core
+// decode (decode_tc.cu) serves the call, fused append included
+bool paged_decode_tc_supported(const DecodeArgs& a);
+cudaError_t launch_paged_decode_tc(const DecodeArgs& a, cudaStream_t stream);
+// 4-D bf16 tensor map over one paged cache tensor [num_blocks, Hkv, 16, 128]
+// (contiguous): box 64 columns x 16 rows of one (block, head), 128-byte swizzle
+bool make_bf16_cache_map(CUtensorMap* map, void* base, int64_t num_blocks, int Hkv);
 
 struct PrefillArgs {
   PagedCache cache;
