@@ -225,7 +225,12 @@ attn_status kv_append(const attn_kv_cache *cache, const int32_t *block_table, in
  * where token t is read from block block_table[b*bt_stride + t/block_size],
  * slot t % block_size.  L = 0 gives out = 0, lse = -inf.  A context needing
  * more than max_blocks blocks, or a block id outside the cache, sets
- * ATTN_ERR_DEVICE_BOUNDS and that (sequence, head) is written as zeros.
+ * ATTN_ERR_DEVICE_BOUNDS: the context is cut to the table and a block with a
+ * bad id is left out (none of its slots is read), so that sequence's result
+ * is not the attention over its whole context and must be discarded.
+ * At head_dim 128 with at most 8 query heads per KV head the products run on
+ * the tensor cores with the softmax weights rounded to bf16 before P.V (as
+ * attn_fwd does); at head_dim 64 every step is fp32.
  *
  *   q       [batch, Hq, head_dim] bf16 (strided view)
  *   out     [batch, Hq, head_dim] bf16 or f32

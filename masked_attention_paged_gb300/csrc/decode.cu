@@ -29,6 +29,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "decode_common.cuh"
 #include "internal.h"
 
 namespace attn {
@@ -407,28 +408,7 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeP
   __syncthreads();
 
   // ---- combine the warps and write this split's partial (normalised out, log2 LSE)
-  for (int x = threadIdx.x; x < G * D; x += kWarps * 32) {
-    const int hh = x / D, d = x % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, comb[(w * G + hh) * kRec + D]);
-    float lsum = 0.f, osum = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float* rec = comb + (w * G + hh) * kRec;
-        if (rec[D] == -INFINITY) continue;
-        const float sc = fast_exp2(rec[D] - M);
-        lsum = fmaf(sc, rec[D + 1], lsum);
-        osum = fmaf(sc, rec[d], osum);
-      }
-    }
-    const int h = g * G + hh;
-    const int64_t slot = (static_cast<int64_t>(b) * p.Hq + h) * p.n_split + split;
-    const bool empty = !(lsum > 0.f);
-    p.o_part[slot * D + d] = empty ? 0.f : osum / lsum;
-    if (d == 0) p.lse_part[slot] = empty ? -INFINITY : M + __log2f(lsum);
-  }
+  decode_combine_warps<D, G, kWarps>(comb, g, b, split, p.Hq, p.n_split, p.o_part, p.lse_part);
 }
 
 // Merge the splits of each (sequence, head): the LSE rule of the ring-attention

@@ -28,6 +28,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "decode_common.cuh"
 #include "internal.h"
 
 namespace attn {
@@ -347,28 +348,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) paged_decode_tc_kernel(const _
   __syncthreads();
 
   // ---- combine the warps, write this split's partial (normalised out, log2 LSE)
-  for (int x = threadIdx.x; x < G * kD; x += kWarps * 32) {
-    const int hh = x / kD, d = x % kD;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, comb[(w * G + hh) * kRec + kD]);
-    float lsum = 0.f, osum = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float* rec = comb + (w * G + hh) * kRec;
-        if (rec[kD] == -INFINITY) continue;
-        const float sc = fast_exp2(rec[kD] - M);
-        lsum = fmaf(sc, rec[kD + 1], lsum);
-        osum = fmaf(sc, rec[d], osum);
-      }
-    }
-    const int h = gkv * G + hh;
-    const int64_t slot = (static_cast<int64_t>(b) * p.Hq + h) * p.n_split + split;
-    const bool empty = !(lsum > 0.f);
-    p.o_part[slot * kD + d] = empty ? 0.f : osum / lsum;
-    if (d == 0) p.lse_part[slot] = empty ? -INFINITY : M + __log2f(lsum);
-  }
+  decode_combine_warps<kD, G, kWarps>(comb, gkv, b, split, p.Hq, p.n_split, p.o_part, p.lse_part);
 }
 
 constexpr size_t tc_decode_smem() {
