@@ -340,7 +340,9 @@ __global__ void __launch_bounds__(kWarps * 32, 4) paged_decode_q8_mma_kernel(con
       um = fmaxf(um, __shfl_xor_sync(0xffffffffu, um, 2));
       // keep w = u / ref in [0, 2^8]: a larger block moves the reference and
       // rescales the output columns of its head (held by the lanes t = h / 2)
-      const bool grow = um > ref * 256.f;
+      // (weights below 1e-30 never set the reference: their reciprocal would
+      // overflow, and next to l >= 1 they are nothing)
+      const bool grow = um > fmaxf(ref * 256.f, 1e-30f);
       if (__any_sync(0xffffffffu, grow)) {
         const float gam = grow ? ref / um : 1.f;
         if (grow) {

@@ -115,7 +115,7 @@ def test_q8_decode_tracks_the_bf16_decode():
     assert err.max().item() < 3e-2 and err.mean().item() < 3e-3
 
 
-def _decode_only_check(d, scale, note):
+def _decode_only_check(d, scale, note, abs_floor=0.0):
     """Decode the cache as given (no append) with float32 output, against the
     oracle within a bound taken from the arithmetic: a softmax weight rounded
     to fp16 is off by at most 2^-11 of itself, so an output element is off by
@@ -131,7 +131,7 @@ def _decode_only_check(d, scale, note):
     ro, rl = oracle.paged_decode_q8(d.q, kq, vq, ks, vs, d.block_table, d.ctx, scale)
     ra, _ = oracle.paged_decode_q8(d.q, kq, np.abs(vq), ks, vs, d.block_table, d.ctx, scale)
     err = np.abs(out.cpu().numpy().astype(np.float64) - ro)
-    bound = 2.0 ** -10 * ra + 1e-6 * ra.max()
+    bound = 2.0 ** -10 * ra + 1e-6 * ra.max() + abs_floor
     assert np.all(err <= bound), f"{note}: worst err/bound {(err / bound).max():.3g}"
     assert_lse_close(lse, rl, what="q8 decode lse " + note)
 
@@ -196,3 +196,26 @@ def test_q8_decode_empty_context_and_bad_block():
     lib.paged_decode_attn_q8(g["q"], g["kq_cache"], g["vq_cache"], g["k_scale"], g["v_scale"], bt, lens, d.scale,
                              workspace=ws)
     assert ws.status() == 5
+
+
+def test_q8_decode_subnormal_value_weights():
+    """One 16-token block whose top-scoring token has value scale 0 and whose
+    other tokens score 125 log2 units lower: every value weight p * vs of the
+    block is subnormal.  The value-weight reference must not be set from
+    such a block (1 / ref would overflow and 0 * inf poison the output); the
+    result is finite and matches the oracle (whose output is ~1e-40 here)."""
+    cfg = workloads.DecodeConfig("t", 1, 4, 1, 128, 16, 0, 16, 2)
+    d = workloads.make_decode_inputs_q8(cfg, seed=59, ctx=[16])
+    blk = int(d.block_table[0, 0])
+    d.kq_cache[blk, 0] = 0
+    d.kq_cache[blk, 0, 0, 0] = 127          # token 0: the only non-zero key
+    d.k_scale[blk, 0] = 0.01
+    d.k_scale[blk, 0, 0] = 125.0 / (127 * d.scale * 1.4426950408889634)  # score 125 (log2) above the rest
+    d.v_scale[blk, 0] = 0.01
+    d.v_scale[blk, 0, 0] = 0.0              # the top token's value row is zero
+    q = torch.zeros_like(d.q.float())
+    q[0, :, 0] = 1.0
+    d.q = q.to(torch.bfloat16)
+    # weights p * vs below 1e-30 are dropped (each token then moves the output
+    # by at most 1e-30 * 127 / l, l >= 1): a floor far below anything visible
+    _decode_only_check(d, d.scale, "subnormal value weights", abs_floor=1e-20)
