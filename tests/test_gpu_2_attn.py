@@ -211,6 +211,21 @@ def test_lse_merge_against_oracle(dtype, n):
     assert_lse_close(ml, full_l)
 
 
+@pytest.mark.parametrize("D,n", [(40, 3), (8, 2), (24, 8)])
+def test_lse_merge_narrow_heads(D, n):
+    """Head dims that are not a multiple of 16 take the 8-elements-per-thread
+    form of the merge: seeded partials (one row fully masked in the first)
+    against the oracle's merge, P with a ragged tail."""
+    g = torch.Generator().manual_seed(60 + D)
+    outs = [torch.randn(2, 3, 77, D, generator=g).to(torch.bfloat16) for _ in range(n)]
+    lses = [(torch.randn(2, 3, 77, generator=g) * 3).float() for _ in range(n)]
+    lses[0][0, 0, 5] = float("-inf")
+    mo, ml = lib.attn_lse_merge([o.to(DEV) for o in outs], [l.to(DEV) for l in lses])
+    ro, rl = oracle.merge([o.float().numpy() for o in outs], [l.numpy() for l in lses])
+    assert_out_close(mo, ro)
+    assert_lse_close(ml, rl)
+
+
 def test_lse_merge_all_partials_masked():
     o = torch.randn(1, 2, 10, 64, device=DEV).to(torch.bfloat16)
     l = torch.full((1, 2, 10), float("-inf"), device=DEV)
