@@ -350,7 +350,9 @@ attn_status kv_append_q8(const attn_kv_cache_q8 *cache, const int32_t *block_tab
  * At head_dim 128 with at most 8 query heads per KV head the products run on
  * the tensor cores: q and the codes enter exactly as fp16, the softmax
  * weights (times the value scales, over a per-head reference) are rounded to
- * fp16, relative error <= 2^-11; elsewhere every step is fp32.
+ * fp16, relative error <= 2^-11, and weights p * vs below 1e-30 are dropped
+ * (p relative to the running max, so each moves an output by at most
+ * 1e-30 * 127 / l, l >= 1); elsewhere every step is fp32.
  * Arguments, workspace size and error behaviour as paged_decode_attn.
  */
 attn_status paged_decode_attn_q8(const attn_tensor *q, const attn_kv_cache_q8 *cache,
