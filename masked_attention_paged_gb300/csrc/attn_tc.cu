@@ -53,6 +53,7 @@
 
 #include <atomic>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -617,7 +618,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float bound = q_l1 * bars->kmax[mb_i] * prm.scale_log2;  // scale > 0 on unmasked tiles
         try_fast = !masked_tile && __all_sync(0xffffffffu, m_run != -INFINITY && bound - m_run <= 60.0f);
       } else {
-        try_fast = !C::kSepP && !masked_tile && __all_sync(0xffffffffu, m_run != -INFINITY);
+        // paged tiles with keys past a row's limit take it too, the keys
+        // selected to -inf before the exponential
+        try_fast = !C::kSepP && (PAGED || !masked_tile) && __all_sync(0xffffffffu, m_run != -INFINITY);
       }
       if (try_fast) {
         float rsum[8];
@@ -625,19 +628,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 8; ++i) rsum[i] = 0.0f;
         const uint64_t sc2 = f2_pack(prm.scale_log2, prm.scale_log2);
         const uint64_t ng2 = f2_pack(-m_run, -m_run);
-        // two keys per packed fma / add; sums in 8 partial accumulators
+        // two keys per packed fma / add; sums in 8 partial accumulators;
+        // LIMIT: keys at or past the row's limit give 0
+        auto fast_loop = [&](auto limit_c) {
+          constexpr bool LIMIT = decltype(limit_c)::value;
 #pragma unroll
-        for (int c = 0; c < kBN; c += 2) {
-          if (c == kFirstLd * 32) finish_ld();
-          float x0, x1;
-          f2_unpack(ffma2(f2_pack(SV(c), SV(c + 1)), sc2, ng2), x0, x1);
-          const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-          sr[c >> 5][c & 31] = __float_as_uint(p0);
-          sr[c >> 5][(c + 1) & 31] = __float_as_uint(p1);
-          const int a = (c >> 1) & 3;
-          uint64_t acc = f2_pack(rsum[a], rsum[4 + a]);
-          f2_unpack(fadd2(acc, f2_pack(p0, p1)), rsum[a], rsum[4 + a]);
-        }
+          for (int c = 0; c < kBN; c += 2) {
+            if (c == kFirstLd * 32) finish_ld();
+            float x0, x1;
+            f2_unpack(ffma2(f2_pack(SV(c), SV(c + 1)), sc2, ng2), x0, x1);
+            if constexpr (LIMIT) {
+              x0 = c < lim ? x0 : -INFINITY;
+              x1 = c + 1 < lim ? x1 : -INFINITY;
+            }
+            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+            sr[c >> 5][c & 31] = __float_as_uint(p0);
+            sr[c >> 5][(c + 1) & 31] = __float_as_uint(p1);
+            const int a = (c >> 1) & 3;
+            uint64_t acc = f2_pack(rsum[a], rsum[4 + a]);
+            f2_unpack(fadd2(acc, f2_pack(p0, p1)), rsum[a], rsum[4 + a]);
+          }
+        };
+        if (PAGED && masked_tile)
+          fast_loop(std::integral_constant<bool, PAGED>());
+        else
+          fast_loop(std::integral_constant<bool, false>());
         rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) + ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
         if (kCert || __all_sync(0xffffffffu, rs <= 18446744073709551616.0f)) {  // 2^64; false for NaN
           done = true;
