@@ -83,6 +83,13 @@ struct Cfg {
   // S one warp issues both tiles in the order PV_A, S_A', PV_B, S_B', which
   // keeps each tile's PV -> next-S chain short.
   static constexpr bool kTwoIssuers = kSepP;
+  // setmaxnreg split of the 168 registers per thread the CTA is launched
+  // with (384 x 168 = 64512): 128 x kRegsCtl + 256 x kRegsSoft must not
+  // exceed it.  At D = 64 the two MMA issuers sit on the critical path and
+  // spilled at 88 (measured: 104 / 200 is 3 % faster than 88 / 208).
+  static constexpr int kRegsCtl = kSepP ? 104 : 88;
+  static constexpr int kRegsSoft = kSepP ? 200 : 208;
+  static_assert(128 * kRegsCtl + 256 * kRegsSoft <= 384 * 168, "register split exceeds the launch allocation");
   static constexpr uint32_t kColP0 = 256 + 2 * D;  // P_A, P_B (kSepP only)
   static constexpr int kBoxes = D / 64;
   static constexpr int kTileBytes = kBM * D * 2;
@@ -272,11 +279,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  // Register budget: launched at 168 per thread (384 x 168 = 64512).  The
-  // producer/MMA/mask warpgroup gives up 80 per thread (10240) and the two
-  // softmax warpgroups take 40 per thread (2 x 128 x 40 = 10240): the sum is
-  // unchanged.
-  if (warp < 4) regs_dec<88>();
+  // Register budget: launched at 168 per thread (384 x 168 = 64512).  At
+  // D = 128 the producer/MMA/mask warpgroup gives up 80 per thread (10240)
+  // and the two softmax warpgroups take 40 (2 x 128 x 40 = 10240); at D = 64
+  // 64 and 32 (8192 each way).
+  if (warp < 4) regs_dec<C::kRegsCtl>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -406,6 +413,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S_t(j+1) as soon as the softmax has read S_t(j), PV_t(j) once P_t(j)
         // is written
         const int t = warp == 1 ? 0 : 1;
+        // Tile B starts once tile A's first P is written.  Started together,
+        // the two tiles run in lockstep: both softmax warpgroups compute at
+        // once while the tensor pipe idles, then both wait for their next S.
+        // Half a step apart, one tile's MMAs overlap the other's softmax.
+        if (ok && t == 1) ok = mbar_wait(&bars->p_full[0], 0, abort, prm.status);
         if (ok) {
           tc_fence_after();
           issue_s(t, 0);
@@ -529,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
-    regs_inc<208>();
+    regs_inc<C::kRegsSoft>();
     const int t = (warp >> 2) - 1;            // query tile 0 (A) or 1 (B)
     const int quarter = warp & 3;             // TMEM lanes this warp may touch
     const int row = quarter * 32 + lane;      // row within the tile == TMEM lane
@@ -1072,11 +1084,11 @@ namespace {
 // softmax warpgroups up to 208) must fit in the registers the launch gives
 // the CTA (threads x registers per thread as compiled); a split that asks for
 // more would wait forever, so a kernel compiled with fewer is never launched.
-template <typename Kern>
+template <int D, typename Kern>
 bool register_split_fits(Kern kern) {
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return false;
-  return 128 * 88 + 256 * 208 <= fa.numRegs * kThreads;
+  return 128 * Cfg<D>::kRegsCtl + 256 * Cfg<D>::kRegsSoft <= fa.numRegs * kThreads;
 }
 
 template <int D, bool OUT_BF16>
@@ -1128,7 +1140,7 @@ cudaError_t launch_tc(const AttnFwdArgs& a, cudaStream_t stream) {
     }
   }
   auto kern = attn_fwd_tc_kernel<D, OUT_BF16, false>;
-  static const bool regs_fit = register_split_fits(kern);
+  static const bool regs_fit = register_split_fits<D>(kern);
   if (!regs_fit) return cudaErrorInvalidConfiguration;
   const int smem = Cfg<D>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -1171,7 +1183,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.lse = a.lse;
   p.status = a.status;
   auto kern = attn_fwd_tc_kernel<D, OUT_BF16, true>;
-  static const bool regs_fit = register_split_fits(kern);
+  static const bool regs_fit = register_split_fits<D>(kern);
   if (!regs_fit) return cudaErrorInvalidConfiguration;
   const int smem = Cfg<D>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
