@@ -1080,10 +1080,11 @@ bool make_code_cache_map(CUtensorMap* map, void* base, int64_t num_blocks, int H
 
 namespace {
 
-// The setmaxnreg split (the control warpgroup down to 88 registers, the two
-// softmax warpgroups up to 208) must fit in the registers the launch gives
-// the CTA (threads x registers per thread as compiled); a split that asks for
-// more would wait forever, so a kernel compiled with fewer is never launched.
+// The setmaxnreg split (the control warpgroup down to Cfg::kRegsCtl
+// registers, the two softmax warpgroups up to kRegsSoft) must fit in the
+// registers the launch gives the CTA (threads x registers per thread as
+// compiled); a split that asks for more would wait forever, so a kernel
+// compiled with fewer is never launched.
 template <int D, typename Kern>
 bool register_split_fits(Kern kern) {
   cudaFuncAttributes fa;
