@@ -55,6 +55,37 @@ class AttnKVCacheQ8(ctypes.Structure):
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
+def _signatures() -> dict:
+    """ctypes result and argument types of every libattn entry point."""
+    P, I32, I64, SZ, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    T = ctypes.POINTER(AttnTensor)
+    C = ctypes.POINTER(AttnKVCache)
+    CQ = ctypes.POINTER(AttnKVCacheQ8)
+    return {
+        "attn_version": (I32, []),
+        "attn_status_string": (ctypes.c_char_p, [I32]),
+        "attn_fwd_workspace_size": (SZ, []),
+        "attn_fwd_workspace_size_for": (SZ, [I32, I32, I64, I32]),
+        "kv_append_workspace_size": (SZ, []),
+        "paged_decode_workspace_size": (SZ, [I32, I32, I32, I32, I32]),
+        "attn_fwd": (I32, [T, T, T, P, I64, F, T, P, P, SZ, P]),
+        "attn_fwd_varlen": (I32, [T, T, T, P, F, T, P, P, SZ, P]),
+        "attn_key_padding_to_additive": (I32, [P, I64, I32, I64, P, I64, P]),
+        "attn_lse_merge": (I32, [I32, T, ctypes.POINTER(P), T, P, P]),
+        "kv_append": (I32, [C, P, I64, I32, P, T, T, P, SZ, P]),
+        "paged_decode_attn": (I32, [T, C, P, I64, I32, P, F, T, P, P, SZ, P]),
+        "paged_decode_attn_append": (I32, [T, T, T, C, P, I64, I32, P, F, T, P, P, SZ, P]),
+        "paged_prefill_attn": (I32, [T, T, T, C, P, I64, I32, P, I32, F, T, P, P, SZ, P]),
+        "kv_append_q8": (I32, [CQ, P, I64, I32, P, T, T, P, SZ, P]),
+        "paged_decode_attn_q8": (I32, [T, CQ, P, I64, I32, P, F, T, P, P, SZ, P]),
+        "paged_kv_gather": (I32, [C, I32, P, I64, I32, P, I32, I64, P, P, SZ, P]),
+        "paged_decode_attn_noalloc": (I32, [T, C, P, I64, I32, P, F, T, P, P, P]),
+        "attn_check_device_status": (I32, [P, ctypes.POINTER(ctypes.c_uint32), P]),
+        "attn_reset_device_status": (I32, [P, P]),
+        "attn_selftest_wait_timeout": (I32, [P, SZ, ctypes.c_uint32, P]),
+    }
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -76,33 +107,7 @@ def load(build_if_missing: bool = False):
                                    "`python -c 'import __graft_entry__ as g; g.build()'`")
             _build.build()
         lib = ctypes.CDLL(path)
-        P, I32, I64, SZ, F = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
-        T = ctypes.POINTER(AttnTensor)
-        C = ctypes.POINTER(AttnKVCache)
-        CQ = ctypes.POINTER(AttnKVCacheQ8)
-        sig = {
-            "attn_version": (I32, []),
-            "attn_status_string": (ctypes.c_char_p, [I32]),
-            "attn_fwd_workspace_size": (SZ, []),
-            "attn_fwd_workspace_size_for": (SZ, [I32, I32, I64, I32]),
-            "kv_append_workspace_size": (SZ, []),
-            "paged_decode_workspace_size": (SZ, [I32, I32, I32, I32, I32]),
-            "attn_fwd": (I32, [T, T, T, P, I64, F, T, P, P, SZ, P]),
-            "attn_fwd_varlen": (I32, [T, T, T, P, F, T, P, P, SZ, P]),
-            "attn_key_padding_to_additive": (I32, [P, I64, I32, I64, P, I64, P]),
-            "attn_lse_merge": (I32, [I32, T, ctypes.POINTER(P), T, P, P]),
-            "kv_append": (I32, [C, P, I64, I32, P, T, T, P, SZ, P]),
-            "paged_decode_attn": (I32, [T, C, P, I64, I32, P, F, T, P, P, SZ, P]),
-            "paged_decode_attn_append": (I32, [T, T, T, C, P, I64, I32, P, F, T, P, P, SZ, P]),
-            "paged_prefill_attn": (I32, [T, T, T, C, P, I64, I32, P, I32, F, T, P, P, SZ, P]),
-            "kv_append_q8": (I32, [CQ, P, I64, I32, P, T, T, P, SZ, P]),
-            "paged_decode_attn_q8": (I32, [T, CQ, P, I64, I32, P, F, T, P, P, SZ, P]),
-            "paged_kv_gather": (I32, [C, I32, P, I64, I32, P, I32, I64, P, P, SZ, P]),
-            "paged_decode_attn_noalloc": (I32, [T, C, P, I64, I32, P, F, T, P, P, P]),
-            "attn_check_device_status": (I32, [P, ctypes.POINTER(ctypes.c_uint32), P]),
-            "attn_reset_device_status": (I32, [P, P]),
-            "attn_selftest_wait_timeout": (I32, [P, SZ, ctypes.c_uint32, P]),
-        }
+        sig = _signatures()
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
             fn.restype = res
@@ -132,7 +137,7 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 
 def _desc(t: torch.Tensor) -> AttnTensor:
-    if not t.is_cuda:
+    if not _on_device(t):
         raise ValueError("libattn tensors must be on a CUDA device")
     d = AttnTensor()
     d.data = t.data_ptr()
@@ -157,8 +162,53 @@ def _check(name: str, st: int):
         raise LibAttnError(name, st)
 
 
-def _ptr(t: Optional[torch.Tensor]):
-    return None if t is None else t.data_ptr()
+# Arguments that reach the library as bare pointers (LSE buffers, masks,
+# block tables, per-sequence positions and lengths) carry no shape the C side
+# could check, so their dtype, layout and size are checked here, with real
+# exceptions rather than asserts (which `python -O` would drop, leaving a
+# kernel to read or write past a short buffer), and their device when the
+# pointer is taken.
+def _require(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _on_device(t: torch.Tensor) -> bool:
+    """Whether t lives where the library's kernels can read it."""
+    return t.is_cuda
+
+
+def _ptr(t: Optional[torch.Tensor], name: str = "tensor"):
+    """Device pointer of t (None passes through as NULL)."""
+    if t is None:
+        return None
+    _require(_on_device(t), f"{name} must be on a CUDA device")
+    return t.data_ptr()
+
+
+def _check_f32_buffer(t: torch.Tensor, numel: int, name: str):
+    """float32, contiguous, exactly `numel` elements."""
+    _require(isinstance(t, torch.Tensor), f"{name} must be a torch tensor")
+    _require(t.dtype == torch.float32, f"{name} must be float32, got {t.dtype}")
+    _require(t.is_contiguous(), f"{name} must be contiguous")
+    _require(t.numel() == numel, f"{name} must hold {numel} elements, got {t.numel()}")
+
+
+def _check_int32_vec(t: torch.Tensor, n: int, name: str):
+    """int32 [n], contiguous."""
+    _require(isinstance(t, torch.Tensor), f"{name} must be a torch tensor")
+    _require(t.dtype == torch.int32, f"{name} must be int32, got {t.dtype}")
+    _require(t.dim() == 1 and t.shape[0] == n and t.is_contiguous(), f"{name} must be contiguous [{n}], got "
+             f"{tuple(t.shape)}")
+
+
+def _check_block_table(t: torch.Tensor, batch: int):
+    """int32 [>= batch, max_blocks] with unit stride along a row."""
+    _require(isinstance(t, torch.Tensor), "block_table must be a torch tensor")
+    _require(t.dtype == torch.int32, f"block_table must be int32, got {t.dtype}")
+    _require(t.dim() == 2 and t.shape[0] >= batch and t.stride(1) == 1 and t.stride(0) >= t.shape[1],
+             f"block_table must be [>= {batch}, max_blocks] with contiguous rows, got {tuple(t.shape)} "
+             f"strides {tuple(t.stride())}")
 
 
 class Workspace:
@@ -245,15 +295,18 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, key_pad_mask: Op
     if lse is None and return_lse:
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
     if lse is not None:
-        assert lse.dtype == torch.float32 and lse.is_contiguous() and tuple(lse.shape) == tuple(q.shape[:3])
+        _check_f32_buffer(lse, q.shape[0] * q.shape[1] * q.shape[2], "lse")
     mptr, mstride = None, 0
     if key_pad_mask is not None:
-        assert key_pad_mask.dtype == torch.float32 and key_pad_mask.stride(-1) == 1
-        mptr, mstride = key_pad_mask.data_ptr(), key_pad_mask.stride(0)
+        m = key_pad_mask
+        _require(m.dtype == torch.float32, f"key_pad_mask must be float32 (additive), got {m.dtype}")
+        _require(m.dim() == 2 and tuple(m.shape) == (q.shape[0], k.shape[2]) and m.stride(1) == 1,
+                 f"key_pad_mask must be [{q.shape[0]}, {k.shape[2]}] with contiguous rows, got {tuple(m.shape)}")
+        mptr, mstride = _ptr(m, "key_pad_mask"), m.stride(0)
     ws = workspace or _attn_ws(q, k)
     dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
     st = lib.attn_fwd(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), mptr, mstride, float(scale),
-                      ctypes.byref(do), _ptr(lse), ws.ptr, ws.nbytes, _stream(stream))
+                      ctypes.byref(do), _ptr(lse, "lse"), ws.ptr, ws.nbytes, _stream(stream))
     _check("attn_fwd", st)
     return (out, lse) if return_lse else out
 
@@ -267,15 +320,17 @@ def attn_fwd_varlen(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, key_lens:
     lib = load()
     if scale is None:
         scale = 1.0 / math.sqrt(q.shape[-1])
-    assert key_lens.dtype == torch.int32 and key_lens.is_contiguous() and key_lens.is_cuda
+    _check_int32_vec(key_lens, q.shape[0], "key_lens")
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
     if lse is None and return_lse:
         lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_f32_buffer(lse, q.shape[0] * q.shape[1] * q.shape[2], "lse")
     ws = workspace or _attn_ws(q, k)
     dq, dk, dv, do = _desc(q), _desc(k), _desc(v), _desc(out)
-    st = lib.attn_fwd_varlen(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), key_lens.data_ptr(), float(scale),
-                             ctypes.byref(do), _ptr(lse), ws.ptr, ws.nbytes, _stream(stream))
+    st = lib.attn_fwd_varlen(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), _ptr(key_lens, "key_lens"),
+                             float(scale), ctypes.byref(do), _ptr(lse, "lse"), ws.ptr, ws.nbytes, _stream(stream))
     _check("attn_fwd_varlen", st)
     return (out, lse) if return_lse else out
 
@@ -286,15 +341,17 @@ def key_padding_to_additive(key_padding_mask: torch.Tensor, out: Optional[torch.
     nn.MultiheadAttention convention) -> float32 additive mask (-inf / 0)."""
     lib = load()
     kpm = key_padding_mask
-    assert kpm.dim() == 2 and kpm.is_cuda and kpm.stride(1) == 1
+    _require(kpm.dim() == 2 and kpm.stride(1) == 1, "key_padding_mask must be [B, Pk] with contiguous rows")
     if kpm.dtype == torch.bool:
         kpm = kpm.view(torch.uint8)
-    assert kpm.dtype == torch.uint8
+    _require(kpm.dtype == torch.uint8, f"key_padding_mask must be bool or uint8, got {kpm.dtype}")
     B, Pk = kpm.shape
     if out is None:
         out = torch.empty(B, Pk, dtype=torch.float32, device=kpm.device)
-    st = lib.attn_key_padding_to_additive(kpm.data_ptr(), kpm.stride(0), B, Pk, out.data_ptr(), out.stride(0),
-                                          _stream(stream))
+    _require(out.dtype == torch.float32 and out.dim() == 2 and tuple(out.shape) == (B, Pk) and out.stride(1) == 1,
+             f"out must be float32 [{B}, {Pk}] with contiguous rows")
+    st = lib.attn_key_padding_to_additive(_ptr(kpm, "key_padding_mask"), kpm.stride(0), B, Pk, _ptr(out, "out"),
+                                          out.stride(0), _stream(stream))
     _check("attn_key_padding_to_additive", st)
     return out
 
@@ -304,22 +361,28 @@ def attn_lse_merge(outs: Sequence[torch.Tensor], lses: Sequence[torch.Tensor], o
     """Merge chunk results: lse = log sum_i exp(lse_i), out = sum_i exp(lse_i - lse) out_i."""
     lib = load()
     n = len(outs)
+    _require(n >= 1 and len(lses) == n, f"attn_lse_merge takes n >= 1 outputs and as many LSEs ({n}, {len(lses)})")
     if out is None:
         out = torch.empty(outs[0].shape, dtype=outs[0].dtype, device=outs[0].device)
+    rows = outs[0].shape[0] * outs[0].shape[1] * outs[0].shape[2]  # B * H * P
     if lse is None:
         lse = torch.empty(lses[0].shape, dtype=torch.float32, device=outs[0].device)
+    _check_f32_buffer(lse, rows, "lse")
+    for i, l in enumerate(lses):
+        _check_f32_buffer(l, rows, f"lses[{i}]")
     arr = (AttnTensor * n)(*[_desc(o) for o in outs])
-    for l in lses:
-        assert l.dtype == torch.float32 and l.is_contiguous()
-    lptrs = (ctypes.c_void_p * n)(*[l.data_ptr() for l in lses])
+    lptrs = (ctypes.c_void_p * n)(*[_ptr(l, f"lses[{i}]") for i, l in enumerate(lses)])
     do = _desc(out)
-    st = lib.attn_lse_merge(n, arr, lptrs, ctypes.byref(do), _ptr(lse), _stream(stream))
+    st = lib.attn_lse_merge(n, arr, lptrs, ctypes.byref(do), _ptr(lse, "lse"), _stream(stream))
     _check("attn_lse_merge", st)
     return out, lse
 
 
 def _cache(k_cache: torch.Tensor, v_cache: torch.Tensor) -> AttnKVCache:
-    assert k_cache.shape == v_cache.shape and k_cache.is_contiguous() and v_cache.is_contiguous()
+    _require(k_cache.dim() == 4 and k_cache.shape == v_cache.shape and k_cache.dtype == v_cache.dtype,
+             "K and V caches must be [num_blocks, Hkv, block_size, D] of one dtype")
+    _require(k_cache.is_contiguous() and v_cache.is_contiguous(), "K and V caches must be contiguous")
+    _require(_on_device(k_cache) and _on_device(v_cache), "K and V caches must be on a CUDA device")
     c = AttnKVCache()
     c.k = k_cache.data_ptr()
     c.v = v_cache.data_ptr()
@@ -336,13 +399,14 @@ def kv_append(k_cache: torch.Tensor, v_cache: torch.Tensor, block_table: torch.T
     """Write k_new/v_new [B, Hkv, D] at token position pos[b] of each
     sequence's paged cache (caches [num_blocks, Hkv, block_size, D])."""
     lib = load()
-    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1
-    assert pos.dtype == torch.int32 and pos.is_contiguous()
+    _check_block_table(block_table, k_new.shape[0])
+    _check_int32_vec(pos, k_new.shape[0], "pos")
     ws = workspace or _small_ws(k_cache.device)
     c = _cache(k_cache, v_cache)
     dk, dv = _desc(k_new), _desc(v_new)
-    st = lib.kv_append(ctypes.byref(c), block_table.data_ptr(), block_table.stride(0), block_table.shape[1],
-                       pos.data_ptr(), ctypes.byref(dk), ctypes.byref(dv), ws.ptr, ws.nbytes, _stream(stream))
+    st = lib.kv_append(ctypes.byref(c), _ptr(block_table, "block_table"), block_table.stride(0),
+                       block_table.shape[1], _ptr(pos, "pos"), ctypes.byref(dk), ctypes.byref(dv), ws.ptr,
+                       ws.nbytes, _stream(stream))
     _check("kv_append", st)
 
 
@@ -356,12 +420,14 @@ def paged_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     B, Hq, D = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1
-    assert ctx_lens.dtype == torch.int32 and ctx_lens.is_contiguous()
+    _check_block_table(block_table, B)
+    _check_int32_vec(ctx_lens, B, "ctx_lens")
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
     if lse is None and return_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_f32_buffer(lse, B * Hq, "lse")
     max_blocks = block_table.shape[1]
     need = paged_decode_workspace_size(B, Hq, max_blocks, k_cache.shape[2], D)
     ws = workspace
@@ -369,8 +435,9 @@ def paged_decode_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
         ws = Workspace(need, device=q.device)
     c = _cache(k_cache, v_cache)
     dq, do = _desc(q), _desc(out)
-    st = lib.paged_decode_attn(ctypes.byref(dq), ctypes.byref(c), block_table.data_ptr(), block_table.stride(0),
-                               max_blocks, ctx_lens.data_ptr(), float(scale), ctypes.byref(do), _ptr(lse),
+    st = lib.paged_decode_attn(ctypes.byref(dq), ctypes.byref(c), _ptr(block_table, "block_table"),
+                               block_table.stride(0), max_blocks, _ptr(ctx_lens, "ctx_lens"), float(scale),
+                               ctypes.byref(do), _ptr(lse, "lse"),
                                ws.ptr, ws.nbytes, _stream(stream))
     _check("paged_decode_attn", st)
     return (out, lse) if return_lse else out
@@ -387,12 +454,14 @@ def paged_decode_attn_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.
     B, Hq, D = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1
-    assert pos.dtype == torch.int32 and pos.is_contiguous()
+    _check_block_table(block_table, B)
+    _check_int32_vec(pos, B, "pos")
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
     if lse is None and return_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_f32_buffer(lse, B * Hq, "lse")
     max_blocks = block_table.shape[1]
     need = paged_decode_workspace_size(B, Hq, max_blocks, k_cache.shape[2], D)
     ws = workspace
@@ -401,8 +470,9 @@ def paged_decode_attn_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.
     c = _cache(k_cache, v_cache)
     dq, dk, dv, do = _desc(q), _desc(k_new), _desc(v_new), _desc(out)
     st = lib.paged_decode_attn_append(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), ctypes.byref(c),
-                                      block_table.data_ptr(), block_table.stride(0), max_blocks, pos.data_ptr(),
-                                      float(scale), ctypes.byref(do), _ptr(lse), ws.ptr, ws.nbytes,
+                                      _ptr(block_table, "block_table"), block_table.stride(0), max_blocks,
+                                      _ptr(pos, "pos"), float(scale), ctypes.byref(do), _ptr(lse, "lse"), ws.ptr,
+                                      ws.nbytes,
                                       _stream(stream))
     _check("paged_decode_attn_append", st)
     return (out, lse) if return_lse else out
@@ -421,30 +491,36 @@ def paged_prefill_attn(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Te
     B, Hq, T, D = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1
-    assert start_pos.dtype == torch.int32 and start_pos.is_contiguous()
+    _check_block_table(block_table, B)
+    _check_int32_vec(start_pos, B, "start_pos")
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
     if lse is None and return_lse:
         lse = torch.empty((B, Hq, T), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_f32_buffer(lse, B * Hq * T, "lse")
     ws = workspace or _small_ws(q.device)
     c = _cache(k_cache, v_cache)
     dq, do = _desc(q), _desc(out)
     dk = ctypes.byref(_desc(k_new)) if k_new is not None else None
     dv = ctypes.byref(_desc(v_new)) if v_new is not None else None
-    st = lib.paged_prefill_attn(ctypes.byref(dq), dk, dv, ctypes.byref(c), block_table.data_ptr(),
-                                block_table.stride(0), block_table.shape[1], start_pos.data_ptr(), int(bool(causal)),
-                                float(scale), ctypes.byref(do), _ptr(lse), ws.ptr, ws.nbytes, _stream(stream))
+    st = lib.paged_prefill_attn(ctypes.byref(dq), dk, dv, ctypes.byref(c), _ptr(block_table, "block_table"),
+                                block_table.stride(0), block_table.shape[1], _ptr(start_pos, "start_pos"),
+                                int(bool(causal)), float(scale), ctypes.byref(do), _ptr(lse, "lse"), ws.ptr,
+                                ws.nbytes, _stream(stream))
     _check("paged_prefill_attn", st)
     return (out, lse) if return_lse else out
 
 
 def _cache_q8(kq: torch.Tensor, vq: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor) -> AttnKVCacheQ8:
-    assert kq.dtype == torch.int8 and vq.dtype == torch.int8 and kq.shape == vq.shape
-    assert k_scale.dtype == torch.float32 and v_scale.dtype == torch.float32
-    assert tuple(k_scale.shape) == tuple(kq.shape[:3]) and tuple(v_scale.shape) == tuple(kq.shape[:3])
+    _require(kq.dtype == torch.int8 and vq.dtype == torch.int8, "INT8 caches must be int8")
+    _require(kq.dim() == 4 and kq.shape == vq.shape, "INT8 caches must be [num_blocks, Hkv, block_size, D], "
+             "K and V alike")
+    _require(k_scale.dtype == torch.float32 and v_scale.dtype == torch.float32, "INT8 row scales must be float32")
+    _require(tuple(k_scale.shape) == tuple(kq.shape[:3]) and tuple(v_scale.shape) == tuple(kq.shape[:3]),
+             f"INT8 row scales must be {tuple(kq.shape[:3])}")
     for t in (kq, vq, k_scale, v_scale):
-        assert t.is_contiguous()
+        _require(t.is_contiguous() and _on_device(t), "INT8 caches and scales must be contiguous CUDA tensors")
     c = AttnKVCacheQ8()
     c.k, c.v, c.k_scale, c.v_scale = kq.data_ptr(), vq.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr()
     c.num_blocks, c.num_kv_heads, c.block_size, c.head_dim = kq.shape
@@ -458,13 +534,14 @@ def kv_append_q8(kq_cache: torch.Tensor, vq_cache: torch.Tensor, k_scale: torch.
     """Quantise each sequence's new K/V rows (bf16 [B, Hkv, D]) to INT8 codes
     with one float32 scale per row and write them at pos[b]."""
     lib = load()
-    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1
-    assert pos.dtype == torch.int32 and pos.is_contiguous()
+    _check_block_table(block_table, k_new.shape[0])
+    _check_int32_vec(pos, k_new.shape[0], "pos")
     ws = workspace or _small_ws(kq_cache.device)
     c = _cache_q8(kq_cache, vq_cache, k_scale, v_scale)
     dk, dv = _desc(k_new), _desc(v_new)
-    st = lib.kv_append_q8(ctypes.byref(c), block_table.data_ptr(), block_table.stride(0), block_table.shape[1],
-                          pos.data_ptr(), ctypes.byref(dk), ctypes.byref(dv), ws.ptr, ws.nbytes, _stream(stream))
+    st = lib.kv_append_q8(ctypes.byref(c), _ptr(block_table, "block_table"), block_table.stride(0),
+                          block_table.shape[1], _ptr(pos, "pos"), ctypes.byref(dk), ctypes.byref(dv), ws.ptr,
+                          ws.nbytes, _stream(stream))
     _check("kv_append_q8", st)
 
 
@@ -479,12 +556,14 @@ def paged_decode_attn_q8(q: torch.Tensor, kq_cache: torch.Tensor, vq_cache: torc
     B, Hq, D = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1
-    assert ctx_lens.dtype == torch.int32 and ctx_lens.is_contiguous()
+    _check_block_table(block_table, B)
+    _check_int32_vec(ctx_lens, B, "ctx_lens")
     if out is None:
         out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
     if lse is None and return_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_f32_buffer(lse, B * Hq, "lse")
     max_blocks = block_table.shape[1]
     need = paged_decode_workspace_size(B, Hq, max_blocks, kq_cache.shape[2], D)
     ws = workspace
@@ -492,8 +571,9 @@ def paged_decode_attn_q8(q: torch.Tensor, kq_cache: torch.Tensor, vq_cache: torc
         ws = Workspace(need, device=q.device)
     c = _cache_q8(kq_cache, vq_cache, k_scale, v_scale)
     dq, do = _desc(q), _desc(out)
-    st = lib.paged_decode_attn_q8(ctypes.byref(dq), ctypes.byref(c), block_table.data_ptr(), block_table.stride(0),
-                                  max_blocks, ctx_lens.data_ptr(), float(scale), ctypes.byref(do), _ptr(lse),
+    st = lib.paged_decode_attn_q8(ctypes.byref(dq), ctypes.byref(c), _ptr(block_table, "block_table"),
+                                  block_table.stride(0), max_blocks, _ptr(ctx_lens, "ctx_lens"), float(scale),
+                                  ctypes.byref(do), _ptr(lse, "lse"),
                                   ws.ptr, ws.nbytes, _stream(stream))
     _check("paged_decode_attn_q8", st)
     return (out, lse) if return_lse else out
@@ -507,14 +587,16 @@ def paged_kv_gather(cache: torch.Tensor, block_table: torch.Tensor, lens: torch.
     lib = load()
     B = lens.shape[0]
     nb, Hkv, bs, D = cache.shape
-    assert lens.dtype == torch.int32 and lens.is_contiguous()
-    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1
+    _check_int32_vec(lens, B, "lens")
+    _check_block_table(block_table, B)
     if out is None:
         out = torch.zeros((B, Hkv, max_len, D), dtype=cache.dtype, device=cache.device)
+    _require(out.dtype == cache.dtype and tuple(out.shape) == (B, Hkv, max_len, D) and out.is_contiguous(),
+             f"out must be contiguous {cache.dtype} [{B}, {Hkv}, {max_len}, {D}]")
     c = _cache(cache, cache)
     ws = workspace or _small_ws(cache.device)
-    st = lib.paged_kv_gather(ctypes.byref(c), 0, block_table.data_ptr(), block_table.stride(0),
-                             block_table.shape[1], lens.data_ptr(), B, max_len, out.data_ptr(), ws.ptr, ws.nbytes,
+    st = lib.paged_kv_gather(ctypes.byref(c), 0, _ptr(block_table, "block_table"), block_table.stride(0),
+                             block_table.shape[1], _ptr(lens, "lens"), B, max_len, _ptr(out, "out"), ws.ptr, ws.nbytes,
                              _stream(stream))
     _check("paged_kv_gather", st)
     return out
@@ -532,14 +614,20 @@ def paged_decode_attn_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: t
     B, Hq, D = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    assert out is not None, "the no-alloc call writes into a caller buffer"
-    assert block_table.dtype == torch.int32 and block_table.stride(-1) == 1
-    assert ctx_lens.dtype == torch.int32 and ctx_lens.is_contiguous()
+    _require(out is not None, "the no-alloc call writes into a caller buffer: pass out")
+    _check_block_table(block_table, B)
+    _check_int32_vec(ctx_lens, B, "ctx_lens")
+    if lse is not None:
+        _check_f32_buffer(lse, B * Hq, "lse")
+    if device_status is not None:
+        _require(device_status.dtype in (torch.int32, torch.uint32) and device_status.numel() >= 1,
+                 "device_status must be a 32-bit word")
     c = _cache(k_cache, v_cache)
     dq, do = _desc(q), _desc(out)
-    st = lib.paged_decode_attn_noalloc(ctypes.byref(dq), ctypes.byref(c), block_table.data_ptr(),
-                                       block_table.stride(0), block_table.shape[1], ctx_lens.data_ptr(),
-                                       float(scale), ctypes.byref(do), _ptr(lse), _ptr(device_status),
+    st = lib.paged_decode_attn_noalloc(ctypes.byref(dq), ctypes.byref(c), _ptr(block_table, "block_table"),
+                                       block_table.stride(0), block_table.shape[1], _ptr(ctx_lens, "ctx_lens"),
+                                       float(scale), ctypes.byref(do), _ptr(lse, "lse"),
+                                       _ptr(device_status, "device_status"),
                                        _stream(stream))
     _check("paged_decode_attn_noalloc", st)
     return out
