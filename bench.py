@@ -31,6 +31,7 @@ import statistics
 import subprocess
 import sys
 import time
+import types
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -520,12 +521,19 @@ def oracle_sample(seed=0, budget_s=15.0, step=None):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    budget = 10.0
+    # about two minutes of oracle work in all, whatever K, each step at least 2 s
+    budget = max(2.0, min(10.0, 120.0 / max(1, args.steps)))
+    # the step's inputs, drawn once (the same seeded workloads as the GPU arm)
+    A = workloads.ATTN_CONFIGS
+    inputs = types.SimpleNamespace(small=workloads.make_attn_inputs(A["patch_small"], 0),
+                                   large=workloads.make_attn_inputs(A["patch_large"], 0),
+                                   chunk=workloads.make_attn_inputs(A["chunked"], 0),
+                                   dec=workloads.make_decode_inputs(workloads.DECODE_CONFIGS["decode"], 0))
     vals, secs = [], []
     for _ in range(args.warmup):
-        oracle_sample(seed=1, budget_s=1.0)
+        oracle_sample(seed=1, budget_s=1.0, step=inputs)
     for i in range(args.steps):
-        v, s, thr, desc = oracle_sample(seed=100 + i, budget_s=budget)
+        v, s, thr, desc = oracle_sample(seed=100 + i, budget_s=budget, step=inputs)
         vals.append(v)
         secs.append(s)
     value = statistics.mean(vals)
