@@ -42,6 +42,7 @@ def rec(monkeypatch):
     r = _Recorder()
     monkeypatch.setattr(lib, "load", lambda build_if_missing=False: r)
     monkeypatch.setattr(lib, "_on_device", lambda t: True)
+    monkeypatch.setattr(lib, "_default_ws", {})  # the CPU workspaces made here stay here
     return r
 
 
