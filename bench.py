@@ -50,13 +50,20 @@ WORKLOAD = ("hot-path step: patch attention B1 H16 P1944 D64 bf16 (0-64 padded t
 
 
 def peaks():
+    """Roofline denominators: the measured copy bandwidth and bf16 GEMM rate of
+    this GPU model when MEASURED_PEAKS.json is present, else the fallback.
+    The step's kernels run for ~13 ms at a time, too short for the power cap
+    to pull the clocks down (the step's sampled SM clock sits at its maximum),
+    so TFLOP/s fractions are taken against the burst GEMM rate."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             p = json.load(f)
         return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
-                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "source": "measured",
+                "gemm_sm_mhz": (p.get("clocks_under_load") or {}).get("sm_mhz_median")}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback",
+            "gemm_sm_mhz": None}
 
 
 def traffic(kernel):
@@ -453,7 +460,7 @@ def next_rows(step, K, W, pk):
         return e0.elapsed_time(e1) / K
 
     f_ms, v_ms, p_ms, q_ms = time_it(fused), time_it(varlen), time_it(prefill), time_it(decode_q8)
-    peak_t = pk["bf16_tflops_sustained"]
+    peak_t = pk["bf16_tflops"]
     f_gbs = step.decode_bytes / (f_ms * 1e-3) / 1e9
     v_tf = step.flops_large / (v_ms * 1e-3) / 1e12
     p_tf = p_flops / (p_ms * 1e-3) / 1e12
@@ -472,6 +479,98 @@ def next_rows(step, K, W, pk):
                                "ms": p_ms, "tflops": p_tf, "frac": p_tf / peak_t, "launches": 2,
                                "flops": p_flops, "traffic": traffic("attn_fwd_tc_kernel_paged_prefill")},
     }
+
+
+# ---------------------------------------------------------------------------
+# peak extra device memory per call (outside the timed region)
+# ---------------------------------------------------------------------------
+SWEEP_P = (1944, 3952, 7776, 11616, 16000, 32000)
+
+
+def _extra(fn):
+    """(allocator peak, drop in the device's free memory) over one call made
+    by fn, in bytes, beyond what was allocated before it.  The caching
+    allocator is emptied first, so what the call needs comes from fresh
+    device allocations and cudaMemGetInfo sees them too."""
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    torch.cuda.reset_peak_memory_stats()
+    base = torch.cuda.memory_allocated()
+    free0 = torch.cuda.mem_get_info()[0]
+    keep = fn()
+    torch.cuda.synchronize()
+    peak = torch.cuda.max_memory_allocated() - base
+    free1 = torch.cuda.mem_get_info()[0]
+    del keep
+    torch.cuda.empty_cache()
+    return int(peak), int(free0 - free1)
+
+
+def extra_hbm(step):
+    """Device memory each call of the step needs beyond its resident inputs
+    (outputs, LSE, partials and workspace, all allocated for the call through
+    the binding), and the same for patch attention over a sweep of image
+    sizes, fitted with a quadratic in P: a materialised 16 x P x P bf16 score
+    matrix ("MultiheadAttention fast path used 18 GB of VRAM") would put
+    32 B/P^2 into the quadratic term."""
+    lib, dev = step.lib, step.dev
+
+    def attn_call(x, q, k, v, m):
+        c = x.cfg
+        ws = lib.Workspace(lib.attn_fwd_workspace_size_for(c.B, c.Hkv, c.Pk, c.D), device=dev)
+        return (ws,) + tuple(lib.attn_fwd(q, k, v, m, x.scale, workspace=ws))
+
+    def chunked():
+        c = step.chunk
+        ws = lib.Workspace(lib.attn_fwd_workspace_size_for(1, c.cfg.Hkv, c.cfg.Pk, c.cfg.D), device=dev)
+        q = step.c_pq.permute(1, 0, 2).unsqueeze(0)
+        k = step.c_pk.permute(1, 0, 2).unsqueeze(0)
+        v = step.c_pv.permute(1, 0, 2).unsqueeze(0)
+        parts = [lib.attn_fwd(q, k[:, :, lo:hi], v[:, :, lo:hi], None, c.scale, workspace=ws)
+                 for lo, hi in c.cfg.chunk_bounds()]
+        out = torch.empty(c.cfg.Pq, c.cfg.Hq, c.cfg.D, dtype=torch.bfloat16, device=dev)
+        mo, ml = lib.attn_lse_merge([p[0] for p in parts], [p[1] for p in parts],
+                                    out=out.permute(1, 0, 2).unsqueeze(0))
+        return ws, parts, out, ml
+
+    def decode():
+        d = step.dec
+        ws = lib.Workspace(lib.paged_decode_workspace_size(d.cfg.B, d.cfg.Hq, step.bt.shape[1], 16, d.cfg.D),
+                           device=dev)
+        lib.kv_append(step.kc, step.vc, step.bt, step.pos, step.kn, step.vn, workspace=ws)
+        return ws, lib.paged_decode_attn(step.dq, step.kc, step.vc, step.bt, step.lens, d.scale, workspace=ws)
+
+    rows = {}
+    for name, fn, note in (
+            ("patch_small", lambda: attn_call(step.small, step.s_q, step.s_k, step.s_v, step.s_m),
+             "out bf16 + lse + workspace (status, key-tile bounds, last-wave partials)"),
+            ("chunked", chunked, "2 partial outs bf16 + 2 lses + merged out + lse + workspace"),
+            ("patch_large", lambda: attn_call(step.large, step.l_q, step.l_k, step.l_v, step.l_m),
+             "out bf16 + lse + workspace (status, key-tile bounds, last-wave partials)"),
+            ("decode", decode, "out bf16 + workspace (status, split-K partials)")):
+        peak, drop = _extra(fn)
+        rows[name] = {"bytes": peak, "device_free_drop": drop, "what": note}
+    # patch attention B1 H16 D64 over the image sizes of the 18 GB page's table (+16000, 32000)
+    g = torch.Generator(device=dev)
+    g.manual_seed(6)
+    sweep = {}
+    for P in SWEEP_P:
+        q, k, v = (torch.randn(1, 16, P, 64, generator=g, device=dev).to(torch.bfloat16) for _ in range(3))
+        m = torch.zeros(1, P, device=dev)
+        m[:, P - 13:] = float("-inf")
+        x = types.SimpleNamespace(cfg=types.SimpleNamespace(B=1, Hkv=16, Pk=P, D=64), scale=0.125)
+        sweep[P] = _extra(lambda: attn_call(x, q, k, v, m))[0]
+        del q, k, v, m
+    Ps = np.array(SWEEP_P, dtype=np.float64)
+    ys = np.array([sweep[P] for P in SWEEP_P], dtype=np.float64)
+    a2, a1, a0 = np.polyfit(Ps, ys, 2)
+    return {"calls": rows,
+            "sweep_P": {str(P): sweep[P] for P in SWEEP_P},
+            "fit_bytes": {"per_P2": float(a2), "per_P": float(a1), "const": float(a0)},
+            "score_matrix_per_P2": 16 * 2,
+            "linear_in_P": bool(abs(a2) < 0.01 * 32),
+            "method": "torch allocator peak over one call (caching allocator emptied first); device_free_drop "
+                      "= cudaMemGetInfo before - after, in 2 MiB allocator segments"}
 
 
 # ---------------------------------------------------------------------------
@@ -518,6 +617,60 @@ def oracle_sample(seed=0, budget_s=15.0, step=None):
     return flops / dt / 1e12, dt, oracle.num_threads(), desc
 
 
+def oracle_per_config(step, big_rows=16384, seed=0):
+    """The fp64 oracle on the host cores, workload by workload: in full for
+    the tiny fp32 attention, the P1944 patch attention and the 64-sequence
+    decode (the oracle's append included); on `big_rows` seeded query rows
+    over all keys for the chunked T32760 attention (one unsplit call: the
+    definition the two chunks and their merge reproduce) and the P32000
+    patch attention, whose full-size times are extrapolated from the rows
+    and labelled as such.  Returns (table, TFLOP/s over what was run,
+    seconds run, threads)."""
+    import oracle
+    oracle.build()
+    A = workloads.ATTN_CONFIGS
+    tiny = workloads.make_attn_inputs(A["tiny_f32"], seed)
+    rng = np.random.default_rng(seed)
+    table = {}
+    run_f = run_s = 0.0
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    for name, x in (("tiny_f32", tiny), ("patch_small", step.small)):
+        c = x.cfg
+        f = workloads.attn_flops(c.B, c.Hq, c.Pq, c.Pk - x.n_pad, c.D)
+        sec = timed(lambda: oracle.attn(x.q, x.k, x.v, x.mask, x.scale))
+        table[name] = {"sample": "full", "seconds": sec, "gflop": f / 1e9, "tflops": f / sec / 1e12}
+        run_f, run_s = run_f + f, run_s + sec
+    d = step.dec
+    f = 4.0 * d.cfg.Hq * float(d.ctx_lens.to(torch.int64).sum()) * d.cfg.D
+
+    def decode():
+        kc, vc = oracle.kv_append(d.k_cache, d.v_cache, d.block_table, d.pos, d.k_new, d.v_new)
+        oracle.paged_decode(d.q, torch.from_numpy(kc).view(torch.bfloat16), torch.from_numpy(vc).view(torch.bfloat16),
+                            d.block_table, d.ctx_lens, d.scale)
+
+    sec = timed(decode)
+    table["decode"] = {"sample": "full (kv_append + paged decode, 64 sequences)", "seconds": sec,
+                       "gflop": f / 1e9, "tflops": f / sec / 1e12}
+    run_f, run_s = run_f + f, run_s + sec
+    for name, x in (("chunked", step.chunk), ("patch_large", step.large)):
+        c = x.cfg
+        total_rows = c.B * c.Hq * c.Pq
+        rows = np.sort(rng.choice(total_rows, big_rows, replace=False))
+        valid = c.Pk - x.n_pad
+        f = workloads.attn_flops(1, 1, big_rows, valid, c.D)
+        sec = timed(lambda: oracle.attn(x.q, x.k, x.v, x.mask, x.scale, rows=rows))
+        table[name] = {"sample": f"{big_rows} seeded query rows of {total_rows}, all {valid} keys", "seconds": sec,
+                       "gflop": f / 1e9, "tflops": f / sec / 1e12,
+                       "full_size_seconds_extrapolated": sec * total_rows / big_rows}
+        run_f, run_s = run_f + f, run_s + sec
+    return table, run_f / run_s / 1e12, run_s, oracle.num_threads()
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -556,6 +709,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-next", action="store_true", help="skip timing the calls outside the step")
+    ap.add_argument("--no-memory", action="store_true", help="skip the peak extra device memory report")
     args = ap.parse_args()
     rank, world, local = dist_init(args.gpus)
     if args.impl == "reference":
@@ -585,19 +739,29 @@ def main():
     attn_tflops = step.attn_flops / (attn_ms * 1e-3) / 1e12
     dec_gbs = step.decode_bytes / (seg["decode"] * 1e-3) / 1e9
     merge_gbs = step.merge_bytes / (seg["merge"] * 1e-3) / 1e9
-    peak_t = pk["bf16_tflops_sustained"]
+    # the step's kernels run at the burst clock (sampled during the timed region): burst GEMM peak
+    peak_t = pk["bf16_tflops"]
     chunk_tflops = step.flops_chunk / (seg["attn_chunks"] * 1e-3) / 1e12
+    mhz = clk.get("sm_mhz")
+    # time x median SM clock: thousands of SM cycles per call, comparable across clocks
+    kcyc = (lambda ms: round(ms * mhz, 1)) if mhz else (lambda ms: None)
+    tf = {n: f / (seg[s] * 1e-3) / 1e12 for n, f, s in (("patch_small", step.flops_small, "attn_small"),
+                                                        ("chunked", step.flops_chunk, "attn_chunks"),
+                                                        ("patch_large", step.flops_large, "attn_large"))}
     rows = {
         "attn_fwd": {"ms": attn_ms, "tflops": attn_tflops, "frac": attn_tflops / peak_t,
-                     "patch_small_tflops": step.flops_small / (seg["attn_small"] * 1e-3) / 1e12,
-                     "chunk_tflops": step.flops_chunk / (seg["attn_chunks"] * 1e-3) / 1e12,
-                     "patch_large_tflops": step.flops_large / (seg["attn_large"] * 1e-3) / 1e12,
+                     "patch_small_tflops": tf["patch_small"], "patch_small_frac": tf["patch_small"] / peak_t,
+                     "patch_small_kcycles": kcyc(seg["attn_small"]),
+                     "chunk_tflops": tf["chunked"], "chunk_frac": tf["chunked"] / peak_t,
+                     "chunk_kcycles": kcyc(seg["attn_chunks"]),
+                     "patch_large_tflops": tf["patch_large"], "patch_large_frac": tf["patch_large"] / peak_t,
+                     "patch_large_kcycles": kcyc(seg["attn_large"]),
                      "patch_large_traffic": traffic("attn_fwd_tc_kernel_patch_large")},
         "paged_decode_attn": {"ms": seg["decode"], "kv_gbs": step.kv_bytes / (seg["decode"] * 1e-3) / 1e9,
-                              "gbs": dec_gbs, "frac": dec_gbs / pk["hbm_gbs"]},
-        "kv_append": {"ms": seg["append"]},
+                              "gbs": dec_gbs, "frac": dec_gbs / pk["hbm_gbs"], "kcycles": kcyc(seg["decode"])},
+        "kv_append": {"ms": seg["append"], "kcycles": kcyc(seg["append"])},
         "attn_lse_merge": {"ms": seg["merge"], "gbs": merge_gbs, "frac": merge_gbs / pk["hbm_gbs"],
-                           "traffic": traffic("lse_merge_kernel")},
+                           "kcycles": kcyc(seg["merge"]), "traffic": traffic("lse_merge_kernel")},
     }
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -610,7 +774,10 @@ def main():
         "roofline": {"bound": "tensor", "kernel": "attn_fwd_tc_kernel<D=128> (chunked workload, 2 launches/step)",
                      "achieved": chunk_tflops, "peak": peak_t, "unit": "TFLOP/s", "frac": chunk_tflops / peak_t,
                      "traffic": traffic("attn_fwd_tc_kernel"),
-                     "peak_source": f"{pk['source']} bf16 sustained (kernel timed inside a long step)",
+                     "peak_source": (f"{pk['source']} bf16 burst GEMM rate (the step runs ~13 ms at a time at the "
+                                     f"burst clock: median {mhz} MHz sampled here; the sustained figure "
+                                     f"{pk['bf16_tflops_sustained']} was taken at {pk['gemm_sm_mhz']} MHz)"),
+                     "sm_mhz": mhz, "kcycles_per_launch": kcyc(seg["attn_chunks"] / 2),
                      "work_per_launch": "4*T*Pk*H*D = 6.594 TFLOP (T 32760, Pk 16380, H 24, D 128)"},
         "decode": {"bound": "hbm", "kernel": "paged_decode_tc_kernel", "achieved": dec_gbs, "peak": pk["hbm_gbs"],
                    "unit": "GB/s", "frac": dec_gbs / pk["hbm_gbs"], "traffic": traffic("paged_decode_tc_kernel"),
@@ -620,6 +787,8 @@ def main():
         "gpu_launches": step.launches_per_step * args.steps,
     }
     step.decode_ms_ref = seg["append"] + seg["decode"]
+    if not args.no_memory:
+        line["peak_extra_hbm"] = extra_hbm(step)
     if not args.no_next:
         line["next"] = next_rows(step, max(5, args.steps // 2), max(3, args.warmup), pk)
     if not args.no_e2e:
@@ -628,9 +797,16 @@ def main():
         line["e2e"] = {"value": world * step.step_flops / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, s, thr, desc = oracle_sample(seed=0, budget_s=15.0, step=step)
-        line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": desc,
-                                "seconds": s}
+        table, v, s, thr = oracle_per_config(step)
+        full = sum(table[n].get("full_size_seconds_extrapolated", table[n]["seconds"])
+                   for n in ("patch_small", "decode", "chunked", "patch_large"))
+        line["cpu_baseline"] = {
+            "value": v, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+            "sample": ("fp64 oracle per workload: tiny_f32, patch_small P1944 and the 64-sequence decode in full; "
+                       "16384 seeded query rows of chunked T32760 and of patch_large P32000 over all keys"),
+            "seconds": s, "per_config": table,
+            "step_seconds_extrapolated": full,
+            "gpu_step_ms": ms_max}
     if rank == 0:
         print(json.dumps(line), flush=True)
     barrier(world)
