@@ -142,13 +142,20 @@ def test_key_bound_path_at_its_threshold(gain):
     k[:, :, 4096:] *= gain
     inp.k = k.to(torch.bfloat16)
     o, l = _run(inp, bounds=True)
-    rows = sample_rows(1, 16, 8192, 64, seed=12)
+    rows = sample_rows(1, 16, 8192, 256, seed=12)
     ro, rl = oracle.attn(inp.q, inp.k, inp.v, inp.mask, inp.scale, rows=rows)
     g = o.reshape(-1, 64)[torch.from_numpy(rows).to(DEV)].float().cpu().numpy()
+    assert_lse_close(l.reshape(-1)[torch.from_numpy(rows).to(DEV)], rl)
+    if gain == 1.0:
+        # ordinary N(0, 1) inputs: the bf16 bars as stated
+        assert_out_close(g, ro, what="key-bound path, gain 1")
+        return
+    # later tiles scaled up: peaked rows, where the bound grows with |ref|
+    # (see test_score_jump_after_the_first_tile)
     err = np.abs(g - ro)
     assert np.all(np.isfinite(g))
     assert np.all(err <= 2e-2 + np.abs(ro) / 256), f"gain {gain}: max abs err {err.max():.3g}"
-    assert_lse_close(l.reshape(-1)[torch.from_numpy(rows).to(DEV)], rl)
+    assert err.mean() <= 2e-3 + np.abs(ro).mean() / 256
 
 
 @pytest.mark.parametrize("D", [64, 128])
@@ -178,10 +185,11 @@ def test_patch_small_workload_full():
 
 
 def test_patch_large_workload_sampled():
-    """B1 H16 P32000 D64 bf16, last 128 keys padded: 96 seeded query rows."""
+    """B1 H16 P32000 D64 bf16, last 128 keys padded: 2048 seeded query rows
+    (the split last wave's rows among them)."""
     inp = workloads.make_attn_inputs(workloads.ATTN_CONFIGS["patch_large"], seed=0)
     o, l = _run(inp, bounds=True)  # the workspace bench.py gives it
-    rows = sample_rows(1, 16, 32000, 96, seed=11)
+    rows = sample_rows(1, 16, 32000, 2048, seed=11)
     ro, rl = oracle.attn(inp.q, inp.k, inp.v, inp.mask, inp.scale, rows=rows)
     assert_out_close(o.reshape(-1, 64)[torch.from_numpy(rows).to(DEV)], ro)
     assert_lse_close(l.reshape(-1)[torch.from_numpy(rows).to(DEV)], rl)
@@ -236,7 +244,8 @@ def test_lse_merge_all_partials_masked():
 def test_chunked_packed_workload_sampled():
     """Packed [T=32760, H=24, D=128] bf16, two KV chunks of 16380 keys each
     attended with their LSE, merged on the GPU, against the oracle over all
-    keys at 64 seeded rows; the merge also matches the unsplit GPU call."""
+    keys at 2048 seeded rows (the split last wave's among them); the merge
+    also matches the unsplit GPU call."""
     cfg = workloads.ATTN_CONFIGS["chunked"]
     inp = workloads.make_attn_inputs(cfg, seed=0)
     q, k, v = inp.q.to(DEV), inp.k.to(DEV), inp.v.to(DEV)  # [1, H, T, D] views of [T, H, D]
@@ -249,7 +258,7 @@ def test_chunked_packed_workload_sampled():
     # packed output buffer [T, H, D] viewed as [1, H, T, D]
     out_packed = torch.empty(cfg.Pq, cfg.Hq, cfg.D, dtype=torch.bfloat16, device=DEV)
     mo, ml = lib.attn_lse_merge(outs, lses, out=out_packed.permute(1, 0, 2).unsqueeze(0))
-    rows = sample_rows(1, 24, 32760, 64, seed=12)
+    rows = sample_rows(1, 24, 32760, 2048, seed=12)
     ro, rl = oracle.attn(inp.q, inp.k, inp.v, None, inp.scale, rows=rows)
     ridx = torch.from_numpy(rows).to(DEV)
     assert_out_close(mo.reshape(-1, 128)[ridx] if mo.is_contiguous() else
