@@ -372,7 +372,10 @@ attn_status paged_decode_attn_q8(const attn_tensor *q, const attn_kv_cache_q8 *c
  * and never call an allocator has nowhere to get one.  This call uses a
  * scratch array built into the library instead: 20 MiB per GPU, created when
  * the library's code is loaded onto that GPU and kept until the process
- * exits.  It allocates and frees nothing.
+ * exits.  It allocates and frees nothing.  (With CUDA's lazy module loading,
+ * the default, that load happens at the first use of the library's code on
+ * the GPU, so the 20 MiB may leave the device's free memory during the first
+ * call of this entry point there.)
  *
  *   Arguments and results are those of paged_decode_attn, without the
  *   workspace.  device_status (a device pointer, may be NULL) receives this
@@ -383,8 +386,13 @@ attn_status paged_decode_attn_q8(const attn_tensor *q, const attn_kv_cache_q8 *c
  *   bytes, plus 256); the 64-sequence, 32-head, head_dim 128 decode with
  *   contexts up to 8192 tokens needs 9.51 MB.
  *   The first call on each device looks up the scratch array's device
- *   address (with that device current) and remembers it; make that first
- *   call before any stream capture.
+ *   address (with that device current) and remembers it with the id of the
+ *   current context; make that first call before any stream capture.  After
+ *   a device reset (a new context, into which the library's code is loaded
+ *   again) the next call looks the address up again, so the same rule holds
+ *   for the first call after a reset.
+ *   `stream` must belong to the current device (the scratch is that
+ *   device's): a stream of another device returns ATTN_ERR_INVALID_ARG.
  *   All calls on a device share the scratch.  The call clears the status
  *   word it needs zeroed on its stream; calls whose work overlaps on the GPU
  *   (other streams, other threads) race on the scratch and must be ordered by

@@ -18,6 +18,8 @@
 // its stream before launching.  Two calls whose kernels overlap on the GPU
 // (different streams, or different host threads without ordering) race on the
 // array and produce wrong results; callers must order them.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "internal.h"
@@ -32,22 +34,63 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
 
-std::mutex g_setup_mu;
-void* g_scratch_addr[kMaxDevices] = {};  // device address of the array, per device
+// The array's device address belongs to the context the library's code was
+// loaded into: a device reset (or any new primary context) loads it again,
+// possibly elsewhere.  So the address is remembered together with the unique
+// id of the context it was looked up in, and looked up again when the
+// current context's id differs.
+struct ScratchAddr {
+  unsigned long long ctx_id;
+  void* addr;
+};
 
-// Once per device, with that device current: translate the array's host-side
-// name into its device address.  The host-side symbol is only a handle; a
-// kernel must never be given it directly.
+std::mutex g_setup_mu;
+ScratchAddr g_scratch[kMaxDevices] = {};
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (0 when it cannot be had).
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// With the device current: translate the array's host-side name into its
+// device address, once per (device, context).  The host-side symbol is only a
+// handle; a kernel must never be given it directly.
 attn_status scratch_for_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  const unsigned long long id = current_context_id();
   std::lock_guard<std::mutex> lock(g_setup_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  ScratchAddr& s = g_scratch[dev];
+  if (s.addr == nullptr || id == 0 || s.ctx_id != id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr) return ATTN_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    s.addr = p;
+    // the lookup made the device's primary context current if none was
+    s.ctx_id = current_context_id();
   }
-  *out = g_scratch_addr[dev];
+  *out = s.addr;
   return ATTN_OK;
 }
 
@@ -65,6 +108,11 @@ extern "C" attn_status paged_decode_attn_noalloc(const attn_tensor* q, const att
                                                   cache->head_dim);
   if (need == 0) return ATTN_ERR_INVALID_ARG;
   if (need > kNoAllocScratchBytes) return ATTN_ERR_WORKSPACE;  // larger than the built-in scratch
+  // the scratch address is the current device's: the work must go there too
+  int dev = -1, stream_dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaStreamGetDevice(stream, &stream_dev) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (stream_dev != dev) return ATTN_ERR_INVALID_ARG;
   void* scratch = nullptr;
   attn_status st = scratch_for_current_device(&scratch);
   if (st != ATTN_OK) return st;
