@@ -71,14 +71,17 @@ constexpr int kBoxBytes = kBM * 128;  // one 64-column (128-byte) box of 128 row
 // by more than this; P then stays below 2^8, well inside bf16 and fp32 range.
 constexpr float kRescaleMargin = 8.0f;
 
-template <int D>
+template <int D, bool SEP = (D == 64)>
 struct Cfg {
-  // D = 64 leaves room in TMEM for P apart from S (S_A, S_B 128 columns each,
+  // SEP (D = 64 only): P in its own TMEM columns (S_A, S_B 128 columns each,
   // O_A, O_B 64 each, P_A, P_B 64 each = 512): the next S can then be issued
   // as soon as the softmax has read the current one, and each softmax
-  // warpgroup runs tile after tile without waiting for its PV.  At D = 128
-  // P is written over the first half of its S region instead.
-  static constexpr bool kSepP = (D == 64);
+  // warpgroup runs tile after tile without waiting for its PV; the max pass
+  // is skipped only where precomputed key bounds certify a tile.  Otherwise
+  // P is written over the first half of its S region, and the softmax
+  // exponentiates optimistically and redoes a tile whose row sums fail.
+  static_assert(D == 64 || !SEP, "P apart from S needs D = 64");
+  static constexpr bool kSepP = SEP;
   // With P apart from S each tile gets its own MMA-issuing warp; with P over
   // S one warp issues both tiles in the order PV_A, S_A', PV_B, S_B', which
   // keeps each tile's PV -> next-S chain short.
@@ -205,11 +208,11 @@ __device__ __forceinline__ void coords(const TmaCoordMap& m, int p, int h, int b
   c3 = m.slot_p == 3 ? p : (m.slot_h == 3 ? h : b);
 }
 
-template <int D, bool OUT_BF16, bool PAGED>
+template <int D, bool OUT_BF16, bool PAGED, bool SEP>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
-  using C = Cfg<D>;
+  using C = Cfg<D, SEP>;
   // With P apart from S the softmax skips the max pass on tiles where a
   // bound certifies that no exponential can overflow (see the stager)
   constexpr bool kCert = C::kSepP && !PAGED;
@@ -644,21 +647,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         // LIMIT: keys at or past the row's limit give 0
         auto fast_loop = [&](auto limit_c) {
           constexpr bool LIMIT = decltype(limit_c)::value;
+          if constexpr (C::kSepP) {
+            // P in its own columns, written once PV_t(j-1) has read the last
+            // tile's: the weights stay in registers until then
 #pragma unroll
-          for (int c = 0; c < kBN; c += 2) {
-            if (c == kFirstLd * 32) finish_ld();
-            float x0, x1;
-            f2_unpack(ffma2(f2_pack(SV(c), SV(c + 1)), sc2, ng2), x0, x1);
-            if constexpr (LIMIT) {
-              x0 = c < lim ? x0 : -INFINITY;
-              x1 = c + 1 < lim ? x1 : -INFINITY;
+            for (int c = 0; c < kBN; c += 2) {
+              float x0, x1;
+              f2_unpack(ffma2(f2_pack(SV(c), SV(c + 1)), sc2, ng2), x0, x1);
+              const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              sr[c >> 5][c & 31] = __float_as_uint(p0);
+              sr[c >> 5][(c + 1) & 31] = __float_as_uint(p1);
+              const int a = (c >> 1) & 3;
+              uint64_t acc = f2_pack(rsum[a], rsum[4 + a]);
+              f2_unpack(fadd2(acc, f2_pack(p0, p1)), rsum[a], rsum[4 + a]);
             }
-            const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-            sr[c >> 5][c & 31] = __float_as_uint(p0);
-            sr[c >> 5][(c + 1) & 31] = __float_as_uint(p1);
-            const int a = (c >> 1) & 3;
-            uint64_t acc = f2_pack(rsum[a], rsum[4 + a]);
-            f2_unpack(fadd2(acc, f2_pack(p0, p1)), rsum[a], rsum[4 + a]);
+          } else {
+            // P over S: each 32-key chunk of P goes to TMEM as soon as it is
+            // computed (chunk c lands on columns 16c..16c+15, whose scores
+            // are already in registers), while the scores stay in registers
+            // so that a failed check below can redo the tile from them
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              if (c == kFirstLd) finish_ld();
+              uint32_t pw[16];
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                const int key = c * 32 + i;
+                float x0, x1;
+                f2_unpack(ffma2(f2_pack(SV(key), SV(key + 1)), sc2, ng2), x0, x1);
+                if constexpr (LIMIT) {
+                  x0 = key < lim ? x0 : -INFINITY;
+                  x1 = key + 1 < lim ? x1 : -INFINITY;
+                }
+                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                pw[i >> 1] = pack_bf16x2(p0, p1);
+                const int a = (i >> 1) & 3;
+                uint64_t acc = f2_pack(rsum[a], rsum[4 + a]);
+                f2_unpack(fadd2(acc, f2_pack(p0, p1)), rsum[a], rsum[4 + a]);
+              }
+              tmem_st16(tmem + lane_addr + p_col + c * 16, pw);
+            }
           }
         };
         if (PAGED && masked_tile)
@@ -669,10 +697,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kCert || __all_sync(0xffffffffu, rs <= 18446744073709551616.0f)) {  // 2^64; false for NaN
           done = true;
         } else {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld32(tmem + lane_addr + s_col + c * 32, sr[c]);
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_wait_ld(sr[c]);
+          // the scores are intact in registers; the P just stored is written
+          // over again below, after these stores have landed
+          tmem_wait_st();
         }
       }
       if (!done) {
@@ -774,16 +801,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) chunk_out(c);
         }
-      } else {
-        // fast path passed: now P may be written (over S's columns, or into
-        // P's own columns once PV_t(j-1) has read them)
-        if constexpr (C::kSepP) {
-          if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], (j - 1) & 1, abort, prm.status))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
+      } else if constexpr (C::kSepP) {
+        // fast path passed: P goes to its own columns once PV_t(j-1) has read
+        // them (over S, P is in TMEM already)
+        if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], (j - 1) & 1, abort, prm.status))) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t pw[16];
@@ -1085,14 +1110,14 @@ namespace {
 // registers the launch gives the CTA (threads x registers per thread as
 // compiled); a split that asks for more would wait forever, so a kernel
 // compiled with fewer is never launched.
-template <int D, typename Kern>
+template <int D, bool SEP, typename Kern>
 bool register_split_fits(Kern kern) {
   cudaFuncAttributes fa;
   if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return false;
-  return 128 * Cfg<D>::kRegsCtl + 256 * Cfg<D>::kRegsSoft <= fa.numRegs * kThreads;
+  return 128 * Cfg<D, SEP>::kRegsCtl + 256 * Cfg<D, SEP>::kRegsSoft <= fa.numRegs * kThreads;
 }
 
-template <int D, bool OUT_BF16>
+template <int D, bool OUT_BF16, bool SEP>
 cudaError_t launch_tc(const AttnFwdArgs& a, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
   TcParams p = {};
@@ -1140,10 +1165,10 @@ cudaError_t launch_tc(const AttnFwdArgs& a, cudaStream_t stream) {
       p.part_lse = a.part_ws + rows * D;
     }
   }
-  auto kern = attn_fwd_tc_kernel<D, OUT_BF16, false>;
-  static const bool regs_fit = register_split_fits<D>(kern);
+  auto kern = attn_fwd_tc_kernel<D, OUT_BF16, false, SEP>;
+  static const bool regs_fit = register_split_fits<D, SEP>(kern);
   if (!regs_fit) return cudaErrorInvalidConfiguration;
-  const int smem = Cfg<D>::kSmemBytes;
+  const int smem = Cfg<D, SEP>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int64_t ctas = p.full_units + (units - p.full_units) * p.split;
@@ -1183,10 +1208,10 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.out_stride[2] = a.out.stride[2];
   p.lse = a.lse;
   p.status = a.status;
-  auto kern = attn_fwd_tc_kernel<D, OUT_BF16, true>;
-  static const bool regs_fit = register_split_fits<D>(kern);
+  auto kern = attn_fwd_tc_kernel<D, OUT_BF16, true, (D == 64)>;
+  static const bool regs_fit = register_split_fits<D, (D == 64)>(kern);
   if (!regs_fit) return cudaErrorInvalidConfiguration;
-  const int smem = Cfg<D>::kSmemBytes;
+  const int smem = Cfg<D, (D == 64)>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>((a.T + 2 * kBM - 1) / (2 * kBM)), static_cast<unsigned>(a.Hq),
@@ -1217,8 +1242,14 @@ size_t split_partial_bytes(int D) {
 
 cudaError_t launch_attn_fwd_tc(const AttnFwdArgs& a, cudaStream_t stream) {
   const bool bf16_out = a.out.dtype == ATTN_BF16;
-  if (a.D == 64) return bf16_out ? launch_tc<64, true>(a, stream) : launch_tc<64, false>(a, stream);
-  if (a.D == 128) return bf16_out ? launch_tc<128, true>(a, stream) : launch_tc<128, false>(a, stream);
+  if (a.D == 64) {
+    // with key bounds: P apart from S and the certified max-free tiles;
+    // without: P over S and the optimistic tiles
+    if (a.key_bound != nullptr)
+      return bf16_out ? launch_tc<64, true, true>(a, stream) : launch_tc<64, false, true>(a, stream);
+    return bf16_out ? launch_tc<64, true, false>(a, stream) : launch_tc<64, false, false>(a, stream);
+  }
+  if (a.D == 128) return bf16_out ? launch_tc<128, true, false>(a, stream) : launch_tc<128, false, false>(a, stream);
   return cudaErrorInvalidValue;
 }
 
