@@ -752,6 +752,7 @@ def main():
         "attn_fwd": {"ms": attn_ms, "tflops": attn_tflops, "frac": attn_tflops / peak_t,
                      "patch_small_tflops": tf["patch_small"], "patch_small_frac": tf["patch_small"] / peak_t,
                      "patch_small_kcycles": kcyc(seg["attn_small"]),
+                     "patch_small_traffic": traffic("attn_fwd_tc_kernel_patch_small"),
                      "chunk_tflops": tf["chunked"], "chunk_frac": tf["chunked"] / peak_t,
                      "chunk_kcycles": kcyc(seg["attn_chunks"]),
                      "patch_large_tflops": tf["patch_large"], "patch_large_frac": tf["patch_large"] / peak_t,
