@@ -115,6 +115,7 @@ struct Barriers {
   uint64_t s_free[2], o_done[2];   // kSepP: S read out by the softmax; PV done
   uint64_t m_full[2], m_empty[2];  // mask tile staging (warp 2 -> softmax warps)
   uint64_t o_final[2];
+  uint64_t first_p;                // tile A's issuer has seen its first P (completes once)
   int m_flag[2];                   // tile has a masked key (or keys past Pk)
   float kmax[2];                   // largest |k| element of the tile (score bound)
   uint32_t tmem_base;
@@ -270,6 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&bars->o_final[0], 1);
     mbar_init(&bars->o_final[1], 1);
+    mbar_init(&bars->first_p, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -420,7 +422,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the two tiles run in lockstep: both softmax warpgroups compute at
         // once while the tensor pipe idles, then both wait for their next S.
         // Half a step apart, one tile's MMAs overlap the other's softmax.
-        if (ok && t == 1) ok = mbar_wait(&bars->p_full[0], 0, abort, prm.status);
+        // The wait is on a barrier of its own, which completes once: by the
+        // time it runs, p_full[0] may have moved on by a phase or two, and a
+        // parity wait on it would then wait for a later phase while tile A
+        // needs this issuer's commits to free its K/V stages.
+        if (ok && t == 1) ok = mbar_wait(&bars->first_p, 0, abort, prm.status);
         if (ok) {
           tc_fence_after();
           issue_s(t, 0);
@@ -447,6 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          if (t == 0 && j == 0) mbar_arrive(&bars->first_p);
           tc_fence_after();
           issue_pv(t, j);
           umma_commit(&bars->o_done[t]);
