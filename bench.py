@@ -438,10 +438,9 @@ def next_rows(step, K, W, pk):
                             workspace=step.ws_attn)
 
     def decode_q8():
-        lib.kv_append_q8(q8["kq_cache"], q8["vq_cache"], q8["k_scale"], q8["v_scale"], q8["block_table"], q8["pos"],
-                         q8["k_new"], q8["v_new"], workspace=step.ws_dec)
-        lib.paged_decode_attn_q8(q8["q"], q8["kq_cache"], q8["vq_cache"], q8["k_scale"], q8["v_scale"],
-                                 q8["block_table"], q8["ctx_lens"], dq8.scale, out=q8_out, workspace=step.ws_dec)
+        lib.paged_decode_attn_append_q8(q8["q"], q8["k_new"], q8["v_new"], q8["kq_cache"], q8["vq_cache"],
+                                        q8["k_scale"], q8["v_scale"], q8["block_table"], q8["pos"], dq8.scale,
+                                        out=q8_out, workspace=step.ws_dec)
 
     def prefill():
         lib.paged_prefill_attn(p_q, p_kc, p_vc, p_bt, p_sp, k_new=p_kn, v_new=p_vn, causal=True, scale=pf.scale,
@@ -469,11 +468,12 @@ def next_rows(step, K, W, pk):
                                      "ms": f_ms, "gbs": f_gbs, "frac": f_gbs / pk["hbm_gbs"], "launches": 2},
         "attn_fwd_varlen": {"workload": "patch_large with key lengths (B 1, H 16, P 32000, D 64, 128 padded keys)",
                             "ms": v_ms, "tflops": v_tf, "frac": v_tf / peak_t, "launches": 1},
-        "paged_decode_attn_q8": {"workload": "decode with an INT8 cache (codes + one float32 scale per token row)",
+        "paged_decode_attn_q8": {"workload": "decode with an INT8 cache (codes + one float32 scale per token row): "
+                                             "paged_decode_attn_append_q8, the new token's append included",
                                  "ms": q_ms, "gbs": q8_bytes / (q_ms * 1e-3) / 1e9,
                                  "frac": q8_bytes / (q_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
                                  "speedup_vs_bf16_decode": (step.decode_ms_ref / q_ms) if step.decode_ms_ref else None,
-                                 "launches": 3, "bytes": q8_bytes, "traffic": traffic("paged_decode_q8_mma_kernel")},
+                                 "launches": 2, "bytes": q8_bytes, "traffic": traffic("paged_decode_q8_mma_kernel")},
         "paged_prefill_attn": {"workload": "prefill_chunk (16 seqs x 1024-token causal chunk after U[0, 7168] "
                                            "cached, Hq 32, Hkv 8, D 128)",
                                "ms": p_ms, "tflops": p_tf, "frac": p_tf / peak_t, "launches": 2,

@@ -404,6 +404,30 @@ attn_status paged_decode_attn_noalloc(const attn_tensor *q, const attn_kv_cache 
                                       const attn_tensor *out, float *lse,
                                       uint32_t *device_status, cudaStream_t stream);
 
+/*
+ * paged_decode_attn_append_q8 -- kv_append_q8 and paged_decode_attn_q8 in one
+ * call ("KV cache in nanoVLM": the newest token's K/V join the cache and are
+ * attended in the same step; "LLM inference memory accounting", section 18:
+ * the INT8 cache).  The INT8 counterpart of paged_decode_attn_append:
+ *   pos[b]          the new token's position (the context before it); the
+ *                   result equals kv_append_q8(pos, k_new, v_new) followed by
+ *                   paged_decode_attn_q8 with ctx_lens = pos + 1, the cache's
+ *                   codes and scales bit for bit; pos < 0 marks an idle
+ *                   sequence (nothing written, out = 0, lse = -inf)
+ *   k_new, v_new    [batch, Hkv, head_dim] bf16, 16-byte aligned rows
+ *   the rest        as paged_decode_attn_q8 (same workspace size)
+ * Head dim 128 with Hq / Hkv in {1, 2, 4, 8} runs one decode launch (the
+ * warp whose block holds the new slot quantises the rows) plus the split
+ * merge; other shapes run kv_append_q8's kernel first.  Positions past the
+ * table and bad block ids are reported as ATTN_ERR_DEVICE_BOUNDS in the
+ * workspace status word, as for the two separate calls.
+ */
+attn_status paged_decode_attn_append_q8(const attn_tensor *q, const attn_tensor *k_new,
+                                        const attn_tensor *v_new, const attn_kv_cache_q8 *cache,
+                                        const int32_t *block_table, int64_t bt_stride, int32_t max_blocks,
+                                        const int32_t *pos, float scale, const attn_tensor *out, float *lse,
+                                        void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* Test/debug export: gather the paged cache of every (sequence, KV head) into
  * contiguous dst [batch, num_kv_heads, max_len, head_dim] (bf16), tokens
  * t < lens[b]; rows t >= lens[b] are left untouched.  Bit-exact.

@@ -78,6 +78,7 @@ def _signatures() -> dict:
         "paged_prefill_attn": (I32, [T, T, T, C, P, I64, I32, P, I32, F, T, P, P, SZ, P]),
         "kv_append_q8": (I32, [CQ, P, I64, I32, P, T, T, P, SZ, P]),
         "paged_decode_attn_q8": (I32, [T, CQ, P, I64, I32, P, F, T, P, P, SZ, P]),
+        "paged_decode_attn_append_q8": (I32, [T, T, T, CQ, P, I64, I32, P, F, T, P, P, SZ, P]),
         "paged_kv_gather": (I32, [C, I32, P, I64, I32, P, I32, I64, P, P, SZ, P]),
         "paged_decode_attn_noalloc": (I32, [T, C, P, I64, I32, P, F, T, P, P, P]),
         "attn_check_device_status": (I32, [P, ctypes.POINTER(ctypes.c_uint32), P]),
@@ -122,7 +123,7 @@ def exported_symbols() -> list[str]:
             "attn_check_device_status", "attn_reset_device_status", "attn_status_string", "attn_version",
             "paged_decode_attn_noalloc", "attn_selftest_wait_timeout", "attn_fwd_varlen",
             "attn_key_padding_to_additive", "paged_decode_attn_append", "paged_prefill_attn",
-            "attn_fwd_workspace_size_for", "kv_append_q8", "paged_decode_attn_q8"]
+            "attn_fwd_workspace_size_for", "kv_append_q8", "paged_decode_attn_q8", "paged_decode_attn_append_q8"]
 
 
 # --------------------------------------------------------------------------
@@ -576,6 +577,40 @@ def paged_decode_attn_q8(q: torch.Tensor, kq_cache: torch.Tensor, vq_cache: torc
                                   ctypes.byref(do), _ptr(lse, "lse"),
                                   ws.ptr, ws.nbytes, _stream(stream))
     _check("paged_decode_attn_q8", st)
+    return (out, lse) if return_lse else out
+
+
+def paged_decode_attn_append_q8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, kq_cache: torch.Tensor,
+                                vq_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor,
+                                block_table: torch.Tensor, pos: torch.Tensor, scale: Optional[float] = None,
+                                out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                                return_lse: bool = False, workspace: Optional[Workspace] = None, stream=None):
+    """kv_append_q8(pos, k_new, v_new) and paged_decode_attn_q8 over tokens
+    [0, pos[b]] in one call; k_new, v_new bf16 [B, Hkv, D], pos int32 [B]."""
+    lib = load()
+    B, Hq, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    _check_block_table(block_table, B)
+    _check_int32_vec(pos, B, "pos")
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _check_f32_buffer(lse, B * Hq, "lse")
+    max_blocks = block_table.shape[1]
+    need = paged_decode_workspace_size(B, Hq, max_blocks, kq_cache.shape[2], D)
+    ws = workspace
+    if ws is None or ws.nbytes < need:
+        ws = Workspace(need, device=q.device)
+    c = _cache_q8(kq_cache, vq_cache, k_scale, v_scale)
+    dq, dk, dv, do = _desc(q), _desc(k_new), _desc(v_new), _desc(out)
+    st = lib.paged_decode_attn_append_q8(ctypes.byref(dq), ctypes.byref(dk), ctypes.byref(dv), ctypes.byref(c),
+                                         _ptr(block_table, "block_table"), block_table.stride(0), max_blocks,
+                                         _ptr(pos, "pos"), float(scale), ctypes.byref(do), _ptr(lse, "lse"),
+                                         ws.ptr, ws.nbytes, _stream(stream))
+    _check("paged_decode_attn_append_q8", st)
     return (out, lse) if return_lse else out
 
 

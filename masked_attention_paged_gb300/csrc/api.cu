@@ -452,6 +452,17 @@ attn_status paged_decode_attn_append(const attn_tensor* q, const attn_tensor* k_
                            workspace, workspace_bytes, stream);
 }
 
+attn_status paged_decode_attn_append_q8(const attn_tensor* q, const attn_tensor* k_new, const attn_tensor* v_new,
+                                        const attn_kv_cache_q8* cache, const int32_t* block_table, int64_t bt_stride,
+                                        int32_t max_blocks, const int32_t* pos, float scale, const attn_tensor* out,
+                                        float* lse, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (k_new == nullptr || v_new == nullptr) return ATTN_ERR_INVALID_ARG;
+  attn_status st;
+  if ((st = check_cache_q8(cache)) != ATTN_OK) return st;
+  return paged_decode_impl(q, k_new, v_new, paged_q8(cache), block_table, bt_stride, max_blocks, pos, scale, out,
+                           lse, workspace, workspace_bytes, stream);
+}
+
 attn_status paged_prefill_attn(const attn_tensor* q, const attn_tensor* k_new, const attn_tensor* v_new,
                                const attn_kv_cache* cache, const int32_t* block_table, int64_t bt_stride,
                                int32_t max_blocks, const int32_t* start_pos, int32_t causal, float scale,

@@ -529,6 +529,22 @@ cudaError_t launch_decode_reduce(const DecodeArgs& a, const float* o_part, const
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (paged_decode_tc_supported(a)) return launch_paged_decode_tc(a, stream);
   if (paged_decode_q8_mma_supported(a)) return launch_paged_decode_q8_mma(a, stream);
+  if (a.cache.k_scale != nullptr && a.k_new.data != nullptr) {
+    // this kernel appends to a bf16 cache only: an INT8 cache gets its new
+    // rows from kv_append_q8 first (ctx_lens holds the new positions)
+    AppendArgs ap;
+    ap.cache = a.cache;
+    ap.block_table = a.block_table;
+    ap.bt_stride = a.bt_stride;
+    ap.max_blocks = a.max_blocks;
+    ap.pos = a.ctx_lens;
+    ap.B = a.B;
+    ap.k_new = a.k_new;
+    ap.v_new = a.v_new;
+    ap.status = a.status;
+    const cudaError_t e = launch_kv_append_q8(ap, stream);
+    if (e != cudaSuccess) return e;
+  }
   DecodeParams p;
   p.kc = a.cache.k;
   p.vc = a.cache.v;

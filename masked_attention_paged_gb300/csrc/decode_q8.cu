@@ -30,12 +30,20 @@
 //    which makes every fragment load of K and of V free of bank conflicts.
 // The CTA decomposition, the cross-warp combine and the split merge are those
 // of the FMA decode: split s of 1024 tokens x KV head x sequence per CTA.
+//
+// Fused append ("KV cache in nanoVLM": the newest token's K/V join the cache
+// and are attended in the same step): with k_new set, ctx_lens holds each
+// sequence's new position, and the warp whose block holds it quantises the
+// new K and V rows (the quantiser of kv_append_q8, so the bits are the same)
+// once the block has landed, writes codes and scales over the slot's copy in
+// shared memory and stores them to the cache.
 #include <cuda.h>
 #include <math.h>
 
 #include "common.cuh"
 #include "decode_common.cuh"
 #include "internal.h"
+#include "q8_quant.cuh"
 
 namespace attn {
 namespace {
@@ -53,8 +61,10 @@ constexpr uint32_t kHalfBits = 0x64806480u;  // exponent of 1024 in each half; 0
 struct Q8MmaParams {
   CUtensorMap kmap;  // codes [num_blocks, Hkv, 16, 128] u8, box = one (block, head)
   CUtensorMap vmap;
-  const float* ks;   // [num_blocks, Hkv, 16]
-  const float* vs;
+  float* ks;  // [num_blocks, Hkv, 16]; written by the fused append only
+  float* vs;
+  uint8_t* kq;  // the code caches themselves (the fused append stores the new rows)
+  uint8_t* vq;
   int64_t num_blocks;
   int Hkv;
   int Hq;
@@ -63,7 +73,11 @@ struct Q8MmaParams {
   const int32_t* bt;
   int64_t bt_stride;
   int max_blocks;
-  const int32_t* ctx_lens;
+  const int32_t* ctx_lens;  // or, with k_new set, each sequence's new-token position
+  int len_add;              // 1 with a fused append
+  const uint16_t* k_new;    // fused append: bf16 [B, Hkv, D] rows (null otherwise)
+  const uint16_t* v_new;
+  int64_t kn_stride[2], vn_stride[2];  // batch, head (elements)
   float scale_log2;
   float* o_part;    // [B, Hq, n_split, D]
   float* lse_part;  // [B, Hq, n_split], log2 units
@@ -138,8 +152,8 @@ __global__ void __launch_bounds__(kWarps * 32, 4) paged_decode_q8_mma_kernel(con
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2;  // fragment row: query head of the group (rows >= G are zero)
   const int t = lane & 3;   // fragment column pair
-  int L = p.ctx_lens[b];
-  L = L < 0 ? 0 : L;
+  const int L_req = p.ctx_lens[b] + p.len_add;
+  int L = L_req < 0 ? 0 : L_req;
   if (L > p.max_blocks * kBS) {
     if (threadIdx.x == 0 && split == 0) report(p.status, kStatusBounds);
     L = p.max_blocks * kBS;
@@ -149,6 +163,13 @@ __global__ void __launch_bounds__(kWarps * 32, 4) paged_decode_q8_mma_kernel(con
   const int t_end = min(L, t_begin + kDecodeSplitTokens);
   const int nblk = (t_end - t_begin + kBS - 1) / kBS;
   const int lb0 = t_begin / kBS;
+  // fused append: the new token is the last of the context (when it fits the
+  // table); i_new is this warp's iteration over its block, or -1
+  int i_new = -1;
+  if (p.k_new != nullptr && L_req >= 1 && L_req == L && L - 1 >= t_begin) {
+    const int rel = (L - 1) / kBS - lb0;
+    if (rel % kWarps == warp) i_new = rel / kWarps;
+  }
 
   uint8_t* wcodes = codes + warp * kQ8Stages * 2 * kCodeBytes;
   float* wscl = scl + warp * kQ8Stages * 2 * kBS;
@@ -274,11 +295,37 @@ __global__ void __launch_bounds__(kWarps * 32, 4) paged_decode_q8_mma_kernel(con
       break;
     }
     if (blk >= 0) {
-      const uint8_t* kb = wcodes + s * 2 * kCodeBytes;
-      const uint8_t* vb = kb + kCodeBytes;
-      const float* ksb = wscl + s * 2 * kBS;
-      const float* vsb = ksb + kBS;
+      uint8_t* kb = wcodes + s * 2 * kCodeBytes;
+      uint8_t* vb = kb + kCodeBytes;
+      float* ksb = wscl + s * 2 * kBS;
+      float* vsb = ksb + kBS;
       const int tok0 = (lb0 + warp + kWarps * i) * kBS;
+      if (i == i_new) {
+        // the block has landed: quantise the new token's K and V rows and put
+        // their codes and scales in place of whatever the slot held (lane l
+        // holds dims 4l..4l+3, inside the row's 16-byte chunk l/4, which the
+        // swizzle puts at chunk (l/4) ^ (slot % 8)); store them to the cache
+        const int slot = (L - 1) % kBS;
+        const int64_t row = (static_cast<int64_t>(blk) * p.Hkv + gkv) * kBS + slot;
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          const uint16_t* src = w ? p.v_new + b * p.vn_stride[0] + gkv * p.vn_stride[1]
+                                  : p.k_new + b * p.kn_stride[0] + gkv * p.kn_stride[1];
+          const uint2 raw = *reinterpret_cast<const uint2*>(src + lane * 4);
+          const float x[4] = {bf16lo_to_f32(raw.x), bf16hi_to_f32(raw.x), bf16lo_to_f32(raw.y),
+                              bf16hi_to_f32(raw.y)};
+          uint32_t packed;
+          const float sc = quantise_lane_q8<4>(x, packed);
+          *reinterpret_cast<uint32_t*>((w ? vb : kb) + slot * kD + ((((lane >> 2) ^ (slot & 7))) << 4) +
+                                       (lane & 3) * 4) = packed;
+          *reinterpret_cast<uint32_t*>((w ? p.vq : p.kq) + row * kD + lane * 4) = packed;
+          if (lane == 0) {
+            (w ? vsb : ksb)[slot] = sc;
+            (w ? p.vs : p.ks)[row] = sc;
+          }
+        }
+        __syncwarp();
+      }
 
       // ---- S = Q K^T: n-tile j holds tokens 8 j + tok_of(n)
       float sacc[2][4];
@@ -451,7 +498,7 @@ cudaError_t launch_g(const DecodeArgs& a, const Q8MmaParams& p, cudaStream_t str
 
 bool paged_decode_q8_mma_supported(const DecodeArgs& a) {
   const int64_t G = a.cache.Hkv > 0 ? a.Hq / a.cache.Hkv : 0;
-  return a.cache.k_scale != nullptr && a.cache.D == kD && a.cache.block_size == kBS && a.k_new.data == nullptr &&
+  return a.cache.k_scale != nullptr && a.cache.D == kD && a.cache.block_size == kBS &&
          (G == 1 || G == 2 || G == 4 || G == 8);
 }
 
@@ -460,8 +507,10 @@ cudaError_t launch_paged_decode_q8_mma(const DecodeArgs& a, cudaStream_t stream)
   if (!make_code_cache_map(&p.kmap, a.cache.k, a.cache.num_blocks, a.cache.Hkv) ||
       !make_code_cache_map(&p.vmap, a.cache.v, a.cache.num_blocks, a.cache.Hkv))
     return cudaErrorInvalidValue;
-  p.ks = a.cache.k_scale;
-  p.vs = a.cache.v_scale;
+  p.ks = const_cast<float*>(a.cache.k_scale);
+  p.vs = const_cast<float*>(a.cache.v_scale);
+  p.kq = static_cast<uint8_t*>(a.cache.k);
+  p.vq = static_cast<uint8_t*>(a.cache.v);
   p.num_blocks = a.cache.num_blocks;
   p.Hkv = a.cache.Hkv;
   p.Hq = static_cast<int>(a.Hq);
@@ -472,6 +521,13 @@ cudaError_t launch_paged_decode_q8_mma(const DecodeArgs& a, cudaStream_t stream)
   p.bt_stride = a.bt_stride;
   p.max_blocks = a.max_blocks;
   p.ctx_lens = a.ctx_lens;
+  p.len_add = a.k_new.data != nullptr ? 1 : 0;
+  p.k_new = static_cast<const uint16_t*>(a.k_new.data);
+  p.v_new = static_cast<const uint16_t*>(a.v_new.data);
+  p.kn_stride[0] = a.k_new.stride[0];
+  p.kn_stride[1] = a.k_new.stride[1];
+  p.vn_stride[0] = a.v_new.stride[0];
+  p.vn_stride[1] = a.v_new.stride[1];
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   const size_t n = static_cast<size_t>(a.B) * a.Hq * a.n_split;
   p.o_part = static_cast<float*>(a.partials);
@@ -487,7 +543,7 @@ cudaError_t launch_paged_decode_q8_mma(const DecodeArgs& a, cudaStream_t stream)
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  return launch_decode_reduce(a, p.o_part, p.lse_part, 0, stream);
+  return launch_decode_reduce(a, p.o_part, p.lse_part, p.len_add, stream);
 }
 
 }  // namespace attn

@@ -9,6 +9,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "q8_quant.cuh"
 #include "internal.h"
 
 namespace attn {
@@ -88,22 +89,10 @@ template <int D>
 __device__ __forceinline__ void quantise_row_q8(const uint16_t* src, int8_t* dst, float* scale_out, int lane) {
   constexpr int E = D / 32;  // elements per lane
   float x[E];
-  float a = 0.0f;
 #pragma unroll
-  for (int e = 0; e < E; ++e) {
-    x[e] = __uint_as_float(static_cast<uint32_t>(src[lane * E + e]) << 16);
-    a = fmaxf(a, fabsf(x[e]));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-  const float scale = __fdiv_rn(a, 127.0f);
-  uint32_t packed = 0u;
-#pragma unroll
-  for (int e = 0; e < E; ++e) {
-    float c = scale > 0.0f ? rintf(__fdiv_rn(x[e], scale)) : 0.0f;
-    c = fminf(fmaxf(c, -127.0f), 127.0f);
-    packed |= (static_cast<uint32_t>(static_cast<int32_t>(c)) & 0xffu) << (8 * e);
-  }
+  for (int e = 0; e < E; ++e) x[e] = __uint_as_float(static_cast<uint32_t>(src[lane * E + e]) << 16);
+  uint32_t packed;
+  const float scale = quantise_lane_q8<E>(x, packed);
   if constexpr (E == 4) {
     *reinterpret_cast<uint32_t*>(dst + lane * 4) = packed;
   } else {

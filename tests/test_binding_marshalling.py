@@ -84,9 +84,11 @@ def test_paged_calls(rec):
     sc = torch.zeros(nb, Hkv, 16)
     lib.kv_append_q8(kq, kq, sc, sc, bt, lens, kn, kn, stream=0)
     lib.paged_decode_attn_q8(q, kq, kq, sc, sc, bt, lens, return_lse=True, stream=0)
+    lib.paged_decode_attn_append_q8(q, kn, kn, kq, kq, sc, sc, bt, lens, return_lse=True, stream=0)
     assert [c for c in rec.calls if c != "paged_decode_workspace_size"] == [
         "kv_append", "paged_decode_attn", "paged_decode_attn_append", "paged_prefill_attn", "paged_prefill_attn",
-        "paged_kv_gather", "paged_decode_attn_noalloc", "kv_append_q8", "paged_decode_attn_q8"]
+        "paged_kv_gather", "paged_decode_attn_noalloc", "kv_append_q8", "paged_decode_attn_q8",
+        "paged_decode_attn_append_q8"]
 
 
 def test_workspace_and_status_calls(rec):

@@ -305,3 +305,15 @@ def test_q8_calls_reject(L):
     assert dec(c=_cache_q8(k=None)) == INVALID
     assert dec(ws_bytes=need - 256) == WORKSPACE
     assert dec(q=_t([4, 32, 128], 0)) == UNSUPPORTED  # f32 queries
+    def fused(k=kn, v=kn, c=None, ws_bytes=need):
+        c = c or _cache_q8()
+        q, out = _t([4, 32, 128]), _t([4, 32, 128])
+        return L.paged_decode_attn_append_q8(ctypes.byref(q), None if k is None else ctypes.byref(k),
+                                             None if v is None else ctypes.byref(v), ctypes.byref(c), FAKE, 10, 10,
+                                             FAKE, 0.1, ctypes.byref(out), None, FAKE, ws_bytes, None)
+    assert fused(k=None) == INVALID
+    assert fused(v=None) == INVALID
+    assert fused(k=_t([4, 8, 64])) == INVALID  # head dim differs from the cache
+    assert fused(k=_t([3, 8, 128])) == INVALID  # batch differs from q
+    assert fused(c=_cache_q8(ks=None)) == INVALID
+    assert fused(ws_bytes=need - 256) == WORKSPACE

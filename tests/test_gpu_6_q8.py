@@ -219,3 +219,75 @@ def test_q8_decode_subnormal_value_weights():
     # weights p * vs below 1e-30 are dropped (each token then moves the output
     # by at most 1e-30 * 127 / l, l >= 1): a floor far below anything visible
     _decode_only_check(d, d.scale, "subnormal value weights", abs_floor=1e-20)
+
+
+def _fused_check(d, note=""):
+    """paged_decode_attn_append_q8 against the oracle (its append, then its
+    decode over the dequantised cache) and, bit for bit, against the two
+    separate calls on a copy of the same cache."""
+    g = _dev(d)
+    ws = lib.Workspace(lib.paged_decode_workspace_size(d.cfg.B, d.cfg.Hq, d.block_table.shape[1], 16, d.cfg.D))
+    out, lse = lib.paged_decode_attn_append_q8(g["q"], g["k_new"], g["v_new"], g["kq_cache"], g["vq_cache"],
+                                               g["k_scale"], g["v_scale"], g["block_table"], g["pos"], d.scale,
+                                               return_lse=True, workspace=ws)
+    assert ws.status() == 0
+    kq, vq, ks, vs = oracle.kv_append_q8(d.kq_cache, d.vq_cache, d.k_scale, d.v_scale, d.block_table, d.pos,
+                                         d.k_new, d.v_new)
+    np.testing.assert_array_equal(g["kq_cache"].cpu().numpy(), kq)
+    np.testing.assert_array_equal(g["vq_cache"].cpu().numpy(), vq)
+    np.testing.assert_array_equal(g["k_scale"].cpu().numpy().view(np.int32), ks.view(np.int32))
+    np.testing.assert_array_equal(g["v_scale"].cpu().numpy().view(np.int32), vs.view(np.int32))
+    ro, rl = oracle.paged_decode_q8(d.q, kq, vq, ks, vs, d.block_table, d.ctx_lens, d.scale)
+    assert_out_close(out, ro, what="q8 fused out" + note)
+    assert_lse_close(lse, rl, what="q8 fused lse" + note)
+    h = _dev(d)
+    lib.kv_append_q8(h["kq_cache"], h["vq_cache"], h["k_scale"], h["v_scale"], h["block_table"], h["pos"],
+                     h["k_new"], h["v_new"], workspace=ws)
+    o2, l2 = lib.paged_decode_attn_q8(h["q"], h["kq_cache"], h["vq_cache"], h["k_scale"], h["v_scale"],
+                                      h["block_table"], h["ctx_lens"], d.scale, return_lse=True, workspace=ws)
+    assert torch.equal(out, o2) and torch.equal(lse, l2)
+
+
+@pytest.mark.parametrize("D,G", [(128, 4), (128, 1), (128, 8), (64, 4)])
+def test_q8_fused_append_decode_small(D, G):
+    """Contexts that put the new token at block and split edges (0, 15, 16,
+    1023, 1024 tokens before it); D = 64 runs the append kernel first."""
+    Hkv = 2
+    cfg = workloads.DecodeConfig("f", 9, G * Hkv, Hkv, D, 16, 0, 1500, 4)
+    d = workloads.make_decode_inputs_q8(cfg, seed=61, ctx=[0, 15, 16, 511, 512, 1023, 1024, 1300, 1500])
+    _fused_check(d, f" D={D} G={G}")
+
+
+def test_q8_fused_append_decode_full_workload():
+    d = workloads.make_decode_inputs_q8(workloads.DECODE_CONFIGS["decode"], seed=0)
+    _fused_check(d, " full")
+
+
+def test_q8_fused_idle_and_bad_positions():
+    """pos < 0 is an idle sequence (nothing written, out = 0, lse = -inf); a
+    position past the table is reported (status 5) with nothing written."""
+    cfg = workloads.DecodeConfig("q", 4, 8, 2, 128, 16, 0, 100, 2)
+    d = workloads.make_decode_inputs_q8(cfg, seed=62, ctx=[3, 30, 60, 90])
+    g = _dev(d)
+    pos = g["pos"].clone()
+    pos[1] = -1
+    pos[2] = 16 * d.block_table.shape[1]
+    ws = lib.Workspace(lib.paged_decode_workspace_size(4, 8, d.block_table.shape[1], 16, 128))
+    out, lse = lib.paged_decode_attn_append_q8(g["q"], g["k_new"], g["v_new"], g["kq_cache"], g["vq_cache"],
+                                               g["k_scale"], g["v_scale"], g["block_table"], pos, d.scale,
+                                               return_lse=True, workspace=ws)
+    assert ws.status() == 5
+    assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
+    p2 = d.pos.clone()
+    p2[1] = -1
+    p2[2] = -1
+    kq, vq, ks, vs = oracle.kv_append_q8(d.kq_cache, d.vq_cache, d.k_scale, d.v_scale, d.block_table, p2,
+                                         d.k_new, d.v_new)
+    np.testing.assert_array_equal(g["kq_cache"].cpu().numpy(), kq)
+    np.testing.assert_array_equal(g["vq_cache"].cpu().numpy(), vq)
+    np.testing.assert_array_equal(g["k_scale"].cpu().numpy().view(np.int32), ks.view(np.int32))
+    np.testing.assert_array_equal(g["v_scale"].cpu().numpy().view(np.int32), vs.view(np.int32))
+    sel = [0, 3]
+    ro, rl = oracle.paged_decode_q8(d.q[sel], kq, vq, ks, vs, d.block_table[sel], d.ctx_lens[sel], d.scale)
+    assert_out_close(out[sel], ro, what="q8 fused out, live sequences")
+    assert_lse_close(lse[sel], rl, what="q8 fused lse, live sequences")
