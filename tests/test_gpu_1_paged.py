@@ -119,6 +119,18 @@ def test_paged_decode_long_context():
     _decode_and_check(d, " long")
 
 
+@pytest.mark.parametrize("D", [128, 64])
+@pytest.mark.parametrize("gain", [8.0, 40.0])
+def test_paged_decode_peaked_scores(D, gain):
+    """Queries scaled up so that the scores spread over tens to hundreds of
+    log2 units: the running maximum moves within blocks, across the warps of
+    a split and across splits, and the weights are nearly one-hot."""
+    cfg = workloads.DecodeConfig("p", 4, 8, 2, D, 16, 0, 3000, 4)
+    d = workloads.make_decode_inputs(cfg, seed=87, ctx=[100, 1100, 2100, 3000])
+    d.q = (d.q.float() * gain).to(torch.bfloat16)
+    _decode_and_check(d, f" D={D} gain={gain}")
+
+
 def test_paged_decode_f32_output_and_strided_q():
     cfg = workloads.DecodeConfig("s", 3, 8, 2, 128, 16, 100, 600, 2)
     d = workloads.make_decode_inputs(cfg, seed=8)

@@ -136,6 +136,20 @@ def _decode_only_check(d, scale, note, abs_floor=0.0):
     assert_lse_close(lse, rl, what="q8 decode lse " + note)
 
 
+@pytest.mark.parametrize("gain", [8.0, 40.0])
+def test_q8_decode_peaked_scores(gain):
+    """Queries scaled up (scores over tens to hundreds of log2 units): the
+    running maximum and the value-weight reference move within and across
+    blocks, and the weights are nearly one-hot.  The output is then close to
+    one dequantised V row, whose bf16 rounding alone averages about 1.5e-3,
+    so the check takes the output in float32 against the kernel's arithmetic
+    bound (see _decode_only_check)."""
+    cfg = workloads.DecodeConfig("p", 4, 8, 2, 128, 16, 0, 3000, 4)
+    d = workloads.make_decode_inputs_q8(cfg, seed=58, ctx=[100, 1100, 2100, 3000])
+    d.q = (d.q.float() * gain).to(torch.bfloat16)
+    _decode_only_check(d, d.scale, f"peaked gain={gain}")
+
+
 @pytest.mark.parametrize("G", [2, 4])
 def test_q8_decode_wide_scales(G):
     """Key and value scales spread over 2^-6..2^6 and 2^-13..2^13 of the usual
