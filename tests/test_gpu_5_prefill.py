@@ -52,6 +52,19 @@ def test_prefill_small(D, G, T, causal):
     _check(inp, causal, note=f" D={D} G={G} T={T} causal={causal}")
 
 
+@pytest.mark.parametrize("gain", [6.0, 40.0])
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_peaked_scores(D, gain):
+    """Queries scaled up so that a later key tile's scores exceed the running
+    maximum by tens to hundreds of log2 units: the optimistic tiles' row-sum
+    check fails and they are redone on the full path (causal, so the row
+    limits apply too)."""
+    cfg = workloads.PrefillConfig("p", 3, 8, 2, D, 260, 16, 0, 0, 2, True)
+    inp = workloads.make_prefill_inputs(cfg, seed=24, start=[0, 129, 700])
+    inp.q = (inp.q.float() * gain).to(torch.bfloat16)
+    _check(inp, True, note=f" peaked D={D} gain={gain}")
+
+
 def test_prefill_f32_output_and_preloaded_chunk():
     """out in f32, and k_new / v_new omitted: the chunk is already cached."""
     cfg = workloads.PrefillConfig("f", 3, 8, 2, 128, 200, 16, 0, 0, 2, True)
