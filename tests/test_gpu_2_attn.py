@@ -234,6 +234,28 @@ def test_lse_merge_narrow_heads(D, n):
     assert_lse_close(ml, rl)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_lse_merge_extreme_lse_spread(dtype):
+    """Partials whose LSEs differ by hundreds to a thousand (far past where
+    exp of either would overflow or underflow on its own), mixed with -inf
+    partials: the merge subtracts the row maximum first, so the result is the
+    dominant partial wherever one dominates and a finite mix elsewhere."""
+    g = torch.Generator().manual_seed(88)
+    n, D = 4, 128
+    outs = [torch.randn(1, 3, 150, D, generator=g).to(dtype) for _ in range(n)]
+    base = torch.randn(1, 3, 150, generator=g) * 2
+    offs = [0.0, -700.0, 350.0, 1000.0]
+    lses = [(base + off + torch.randn(1, 3, 150, generator=g)).float() for off in offs]
+    lses[3][0, 0, :50] = float("-inf")   # the largest partial absent on some rows
+    lses[2][0, 1, ::3] = float("-inf")
+    lses[1][0, 2, :] = 1000.0 + base[0, 2]  # a tie with partial 3 on one head
+    lses[3][0, 2, :] = 1000.0 + base[0, 2]
+    mo, ml = lib.attn_lse_merge([o.to(DEV) for o in outs], [l.to(DEV) for l in lses])
+    ro, rl = oracle.merge([o.float().numpy() for o in outs], [l.numpy() for l in lses])
+    assert_out_close(mo, ro, fp32_inputs=dtype == torch.float32, what="extreme spread")
+    assert_lse_close(ml, rl)
+
+
 def test_lse_merge_all_partials_masked():
     o = torch.randn(1, 2, 10, 64, device=DEV).to(torch.bfloat16)
     l = torch.full((1, 2, 10), float("-inf"), device=DEV)
