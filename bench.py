@@ -220,8 +220,9 @@ class Step:
                              int(((d.ctx_lens.to(torch.int64) + 15) // 16).sum()) * 4)
         self.merge_bytes = 3 * T * H * D * 2 + 3 * H * T * 4
         # attn x4, the P32000 key-bound pass, the last-wave merge of the chunk and P32000 launches (3),
-        # append, decode split + reduce, merge (152-SM GPU: the chunk and P32000 grids end in partial waves)
-        self.launches_per_step = 12
+        # append, decode (its splits merged in the same launch), merge (152-SM GPU: the chunk and P32000
+        # grids end in partial waves)
+        self.launches_per_step = 11
         self.decode_ms_ref = None  # bf16 append + decode time of the step, for the INT8 comparison
 
     @property
@@ -465,7 +466,7 @@ def next_rows(step, K, W, pk):
     p_tf = p_flops / (p_ms * 1e-3) / 1e12
     return {
         "paged_decode_attn_append": {"workload": "decode (64 seqs, Hq 32, Hkv 8, D 128, ctx U[512, 8192])",
-                                     "ms": f_ms, "gbs": f_gbs, "frac": f_gbs / pk["hbm_gbs"], "launches": 2},
+                                     "ms": f_ms, "gbs": f_gbs, "frac": f_gbs / pk["hbm_gbs"], "launches": 1},
         "attn_fwd_varlen": {"workload": "patch_large with key lengths (B 1, H 16, P 32000, D 64, 128 padded keys)",
                             "ms": v_ms, "tflops": v_tf, "frac": v_tf / peak_t, "launches": 1},
         "paged_decode_attn_q8": {"workload": "decode with an INT8 cache (codes + one float32 scale per token row): "
@@ -473,7 +474,7 @@ def next_rows(step, K, W, pk):
                                  "ms": q_ms, "gbs": q8_bytes / (q_ms * 1e-3) / 1e9,
                                  "frac": q8_bytes / (q_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
                                  "speedup_vs_bf16_decode": (step.decode_ms_ref / q_ms) if step.decode_ms_ref else None,
-                                 "launches": 2, "bytes": q8_bytes, "traffic": traffic("paged_decode_q8_mma_kernel")},
+                                 "launches": 1, "bytes": q8_bytes, "traffic": traffic("paged_decode_q8_mma_kernel")},
         "paged_prefill_attn": {"workload": "prefill_chunk (16 seqs x 1024-token causal chunk after U[0, 7168] "
                                            "cached, Hq 32, Hkv 8, D 128)",
                                "ms": p_ms, "tflops": p_tf, "frac": p_tf / peak_t, "launches": 2,

@@ -41,8 +41,26 @@ int decode_num_splits(int max_blocks, int block_size) {
 
 size_t decode_partial_bytes(int64_t B, int64_t Hq, int n_split, int D) {
   const size_t n = static_cast<size_t>(B) * Hq * n_split;
-  size_t bytes = n * D * sizeof(float) + n * sizeof(float);
+  // outputs, log2 LSEs, and one split count per (sequence, KV head) (Hq bounds Hkv)
+  size_t bytes = n * D * sizeof(float) + n * sizeof(float) + static_cast<size_t>(B) * Hq * sizeof(int);
   return (bytes + 255) & ~size_t(255);
+}
+
+SplitMerge decode_split_merge(const DecodeArgs& a, int D) {
+  SplitMerge m;
+  const size_t n = static_cast<size_t>(a.B) * a.Hq * a.n_split;
+  m.o_part = static_cast<float*>(a.partials);
+  m.lse_part = m.o_part + n * D;
+  m.count = reinterpret_cast<int*>(m.lse_part + n);
+  m.n_split = a.n_split;
+  m.Hq = static_cast<int>(a.Hq);
+  m.Hkv = a.cache.Hkv;
+  m.out = a.out.data;
+  m.out_bf16 = a.out.dtype == ATTN_BF16;
+  m.os0 = a.out.stride[0];
+  m.os1 = a.out.stride[1];
+  m.lse = a.lse;
+  return m;
 }
 
 namespace {
@@ -70,10 +88,7 @@ struct DecodeParams {
   const uint16_t* v_new;
   int64_t kn_stride[2], vn_stride[2];  // batch, head
   float scale_log2;
-  float* o_part;    // [B, Hq, n_split, D]
-  float* lse_part;  // [B, Hq, n_split], log2 units
-  int n_split;
-  int Hq;
+  SplitMerge sm;
   uint32_t* status;
 };
 
@@ -132,7 +147,10 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeP
     L = p.max_blocks * kBS;
   }
   const int t_begin = split * kDecodeSplitTokens;
-  if (t_begin >= L) return;  // nothing of this sequence in this split
+  if (t_begin >= L) {  // nothing of this sequence in this split
+    if (split == 0) decode_write_empty<D, G>(p.sm, g, b);
+    return;
+  }
   const int t_end = min(L, t_begin + kDecodeSplitTokens);
   const int nblk = (t_end - t_begin + kBS - 1) / kBS;
   const int lb0 = t_begin / kBS;
@@ -408,82 +426,8 @@ __global__ void __launch_bounds__(kWarps * 32) paged_decode_kernel(const DecodeP
   __syncthreads();
 
   // ---- combine the warps and write this split's partial (normalised out, log2 LSE)
-  decode_combine_warps<D, G, kWarps>(comb, g, b, split, p.Hq, p.n_split, p.o_part, p.lse_part);
-}
-
-// Merge the splits of each (sequence, head): the LSE rule of the ring-attention
-// page, with the LSEs in log2 units.  One warp per (sequence, head): lane s
-// holds split s's LSE (32 splits per pass), the warp max and the weights come
-// from shuffles, and the partial outputs of up to 8 splits are loaded before
-// any is used, so the merge costs a few memory latencies, not one per split.
-template <int D>
-__global__ void decode_reduce_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
-                                     const int32_t* __restrict__ ctx_lens, int len_add, int max_tokens, int n_split,
-                                     int64_t B, int Hq, void* out, int out_bf16, int64_t os0, int64_t os1,
-                                     float* lse) {
-  constexpr int DPL = D / 32;  // dims per lane
-  constexpr int kBatch = 8;    // splits whose outputs are in flight together
-  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= B * Hq) return;
-  const int64_t b = wid / Hq;
-  const int h = static_cast<int>(wid % Hq);
-  int L = ctx_lens[b] + len_add;
-  L = L < 0 ? 0 : (L > max_tokens ? max_tokens : L);
-  const int ns = (L + kDecodeSplitTokens - 1) / kDecodeSplitTokens;
-  const int64_t base = wid * n_split;
-  const float ls0 = lane < ns ? lse_part[base + lane] : -INFINITY;
-  float M = ls0;
-  for (int s0 = 32; s0 < ns; s0 += 32)
-    if (s0 + lane < ns) M = fmaxf(M, lse_part[base + s0 + lane]);
-#pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, m));
-  float acc[DPL];
-#pragma unroll
-  for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
-  float wsum = 0.f;
-  if (M != -INFINITY) {
-    for (int s0 = 0; s0 < ns; s0 += 32) {
-      const float ls = s0 == 0 ? ls0 : (s0 + lane < ns ? lse_part[base + s0 + lane] : -INFINITY);
-      const float w = ls == -INFINITY ? 0.f : fast_exp2(ls - M);
-      wsum += w;
-      const int n = min(32, ns - s0);
-      for (int k0 = 0; k0 < n; k0 += kBatch) {
-        float ov[kBatch][DPL];
-        float wk[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          wk[u] = __shfl_sync(0xffffffffu, w, (k0 + u) & 31);
-          const bool use = k0 + u < n && wk[u] > 0.f;  // empty splits may hold anything
-          const float* op = o_part + (base + s0 + k0 + u) * D + lane * DPL;
-#pragma unroll
-          for (int e = 0; e < DPL; ++e) ov[u][e] = use ? op[e] : 0.f;
-          if (!use) wk[u] = 0.f;
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u)
-#pragma unroll
-          for (int e = 0; e < DPL; ++e) acc[e] = fmaf(wk[u], ov[u][e], acc[e]);
-      }
-    }
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, m);
-  }
-  const bool empty = !(wsum > 0.f);
-  const float inv = empty ? 0.f : 1.f / wsum;
-  const int64_t ob = b * os0 + h * os1 + lane * DPL;
-  if (out_bf16) {
-    uint16_t* dst = static_cast<uint16_t*>(out) + ob;
-#pragma unroll
-    for (int e = 0; e < DPL; e += 2)
-      *reinterpret_cast<uint32_t*>(dst + e) = pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
-  } else {
-    float* dst = static_cast<float*>(out) + ob;
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) dst[e] = acc[e] * inv;
-  }
-  if (lse != nullptr && lane == 0)
-    lse[wid] = empty ? -INFINITY : (M + __log2f(wsum)) * 0.6931471805599453f;
+  decode_combine_warps<D, G, kWarps>(comb, g, b, split, p.sm);
+  decode_finish<D, G, kWarps>(p.sm, g, b, (L + kDecodeSplitTokens - 1) / kDecodeSplitTokens);
 }
 
 template <int D, int G, bool Q8>
@@ -495,9 +439,7 @@ cudaError_t launch_decode(const DecodeArgs& a, const DecodeParams& p, cudaStream
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(a.n_split), static_cast<unsigned>(a.cache.Hkv), static_cast<unsigned>(a.B));
   kern<<<grid, kWarps * 32, smem, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  return launch_decode_reduce(a, p.o_part, p.lse_part, p.len_add, stream);
+  return cudaGetLastError();
 }
 
 template <int D, bool Q8>
@@ -514,17 +456,6 @@ cudaError_t launch_decode_d(const DecodeArgs& a, const DecodeParams& p, cudaStre
 }  // namespace
 
 // host side
-
-cudaError_t launch_decode_reduce(const DecodeArgs& a, const float* o_part, const float* lse_part, int len_add,
-                                 cudaStream_t stream) {
-  const int64_t warps = a.B * a.Hq;
-  const unsigned blocks = static_cast<unsigned>((warps * 32 + 127) / 128);
-  auto kern = a.cache.D == 64 ? decode_reduce_kernel<64> : decode_reduce_kernel<128>;
-  kern<<<blocks, 128, 0, stream>>>(o_part, lse_part, a.ctx_lens, len_add, a.max_blocks * kBS, a.n_split, a.B,
-                                   static_cast<int>(a.Hq), a.out.data, a.out.dtype == ATTN_BF16, a.out.stride[0],
-                                   a.out.stride[1], a.lse);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (paged_decode_tc_supported(a)) return launch_paged_decode_tc(a, stream);
@@ -567,11 +498,7 @@ cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream) {
   p.vn_stride[0] = a.v_new.stride[0];
   p.vn_stride[1] = a.v_new.stride[1];
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-  const size_t n = static_cast<size_t>(a.B) * a.Hq * a.n_split;
-  p.o_part = static_cast<float*>(a.partials);
-  p.lse_part = p.o_part + n * a.cache.D;
-  p.n_split = a.n_split;
-  p.Hq = static_cast<int>(a.Hq);
+  p.sm = decode_split_merge(a, static_cast<int>(a.cache.D));
   p.status = a.status;
   const bool q8 = a.cache.k_scale != nullptr;
   if (a.cache.D == 64) return q8 ? launch_decode_d<64, true>(a, p, stream) : launch_decode_d<64, false>(a, p, stream);

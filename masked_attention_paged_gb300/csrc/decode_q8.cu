@@ -79,9 +79,7 @@ struct Q8MmaParams {
   const uint16_t* v_new;
   int64_t kn_stride[2], vn_stride[2];  // batch, head (elements)
   float scale_log2;
-  float* o_part;    // [B, Hq, n_split, D]
-  float* lse_part;  // [B, Hq, n_split], log2 units
-  int n_split;
+  SplitMerge sm;
   uint32_t* status;
 };
 
@@ -159,7 +157,10 @@ __global__ void __launch_bounds__(kWarps * 32, 4) paged_decode_q8_mma_kernel(con
     L = p.max_blocks * kBS;
   }
   const int t_begin = split * kDecodeSplitTokens;
-  if (t_begin >= L) return;  // nothing of this sequence in this split
+  if (t_begin >= L) {  // nothing of this sequence in this split
+    if (split == 0) decode_write_empty<kD, G>(p.sm, gkv, b);
+    return;
+  }
   const int t_end = min(L, t_begin + kDecodeSplitTokens);
   const int nblk = (t_end - t_begin + kBS - 1) / kBS;
   const int lb0 = t_begin / kBS;
@@ -474,7 +475,8 @@ __global__ void __launch_bounds__(kWarps * 32, 4) paged_decode_q8_mma_kernel(con
   __syncthreads();
 
   // ---- combine the warps, write this split's partial (normalised out, log2 LSE)
-  decode_combine_warps<kD, G, kWarps>(comb, gkv, b, split, p.Hq, p.n_split, p.o_part, p.lse_part);
+  decode_combine_warps<kD, G, kWarps>(comb, gkv, b, split, p.sm);
+  decode_finish<kD, G, kWarps>(p.sm, gkv, b, (L + kDecodeSplitTokens - 1) / kDecodeSplitTokens);
 }
 
 constexpr size_t q8_mma_smem() {
@@ -529,10 +531,7 @@ cudaError_t launch_paged_decode_q8_mma(const DecodeArgs& a, cudaStream_t stream)
   p.vn_stride[0] = a.v_new.stride[0];
   p.vn_stride[1] = a.v_new.stride[1];
   p.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
-  const size_t n = static_cast<size_t>(a.B) * a.Hq * a.n_split;
-  p.o_part = static_cast<float*>(a.partials);
-  p.lse_part = p.o_part + n * kD;
-  p.n_split = a.n_split;
+  p.sm = decode_split_merge(a, kD);
   p.status = a.status;
   cudaError_t e;
   switch (a.Hq / a.cache.Hkv) {
@@ -542,8 +541,7 @@ cudaError_t launch_paged_decode_q8_mma(const DecodeArgs& a, cudaStream_t stream)
     case 8: e = launch_g<8>(a, p, stream); break;
     default: return cudaErrorInvalidValue;
   }
-  if (e != cudaSuccess) return e;
-  return launch_decode_reduce(a, p.o_part, p.lse_part, p.len_add, stream);
+  return e;
 }
 
 }  // namespace attn

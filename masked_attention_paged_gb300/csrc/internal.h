@@ -116,9 +116,11 @@ constexpr int kDecodeSplitTokens = 1024;
 int decode_num_splits(int max_blocks, int block_size);
 size_t decode_partial_bytes(int64_t B, int64_t Hq, int n_split, int D);
 cudaError_t launch_paged_decode(const DecodeArgs& a, cudaStream_t stream);
-// merge the split partials [B, Hq, n_split, D] (+ log2 LSEs) into a.out / a.lse
-cudaError_t launch_decode_reduce(const DecodeArgs& a, const float* o_part, const float* lse_part, int len_add,
-                                 cudaStream_t stream);
+// where the decode kernels' splits meet (decode_common.cuh): the partials and
+// split counts in a.partials, and a.out / a.lse, which the last split of each
+// (sequence, KV head) writes
+struct SplitMerge;
+SplitMerge decode_split_merge(const DecodeArgs& a, int D);
 // INT8 cache, D = 128, 16-token blocks, Hq / Hkv in {1, 2, 4, 8}, no fused append:
 // the tensor-core decode (decode_q8.cu) serves the call
 bool paged_decode_q8_mma_supported(const DecodeArgs& a);
