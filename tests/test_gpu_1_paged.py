@@ -120,6 +120,30 @@ def test_paged_decode_long_context():
 
 
 @pytest.mark.parametrize("D", [128, 64])
+def test_paged_decode_reuses_its_workspace(D):
+    """Three decode calls through one workspace with different context
+    lengths (so each sequence has a different number of splits every time):
+    the split counts that the merging CTA resets must be back at zero for the
+    next call, and every call matches the oracle."""
+    cfg = workloads.DecodeConfig("w", 5, 8, 2, D, 16, 0, 3000, 4)
+    d = workloads.make_decode_inputs(cfg, seed=89, ctx=[3000, 2500, 1024, 700, 5])
+    ek, ev = oracle.kv_append(d.k_cache, d.v_cache, d.block_table, d.pos, d.k_new, d.v_new)
+    kc, vc = torch.from_numpy(ek).view(torch.bfloat16), torch.from_numpy(ev).view(torch.bfloat16)
+    g = {k: getattr(d, k).to(DEV) for k in ("block_table", "q")}
+    gk, gv = kc.to(DEV), vc.to(DEV)
+    ws = lib.Workspace(lib.paged_decode_workspace_size(cfg.B, cfg.Hq, d.block_table.shape[1], 16, D))
+    full = d.ctx_lens.clone()
+    for lens in (full, torch.clamp(full - 1100, min=0), torch.tensor([1, 1025, 2049, 3001, 0], dtype=torch.int32)):
+        lens = torch.minimum(lens.to(torch.int32), full)
+        out, lse = lib.paged_decode_attn(g["q"], gk, gv, g["block_table"], lens.to(DEV), d.scale, return_lse=True,
+                                         workspace=ws)
+        assert ws.status() == 0
+        ro, rl = oracle.paged_decode(d.q, kc, vc, d.block_table, lens, d.scale)
+        assert_out_close(out, ro, what=f"reused workspace, lens {lens.tolist()}")
+        assert_lse_close(lse, rl)
+
+
+@pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("gain", [8.0, 40.0])
 def test_paged_decode_peaked_scores(D, gain):
     """Queries scaled up so that the scores spread over tens to hundreds of
