@@ -627,6 +627,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float alpha = 1.0f;
       float rs = 0.0f;
       bool done = false;
+      // P apart from S: the weights as bf16 pairs, packed before the wait for
+      // PV_t(j-1) that frees P's columns
+      uint32_t pws[C::kSepP ? 4 : 1][16];
       // Fast path: exponentiate against the current reference max without a
       // max pass.  P over S: every term is <= 2^64 exactly when the row sum
       // is, which keeps the sums far from fp32 overflow; if some row fails,
@@ -653,17 +656,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // two keys per packed fma / add; sums in 8 partial accumulators;
         // LIMIT: keys at or past the row's limit give 0
         auto fast_loop = [&](auto limit_c) {
-          constexpr bool LIMIT = decltype(limit_c)::value;
+          [[maybe_unused]] constexpr bool LIMIT = decltype(limit_c)::value;
           if constexpr (C::kSepP) {
             // P in its own columns, written once PV_t(j-1) has read the last
-            // tile's: the weights stay in registers until then
+            // tile's: the weights wait in registers, packed as bf16 pairs
 #pragma unroll
             for (int c = 0; c < kBN; c += 2) {
               float x0, x1;
               f2_unpack(ffma2(f2_pack(SV(c), SV(c + 1)), sc2, ng2), x0, x1);
               const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
-              sr[c >> 5][c & 31] = __float_as_uint(p0);
-              sr[c >> 5][(c + 1) & 31] = __float_as_uint(p1);
+              pws[c >> 5][(c & 31) >> 1] = pack_bf16x2(p0, p1);
               const int a = (c >> 1) & 3;
               uint64_t acc = f2_pack(rsum[a], rsum[4 + a]);
               f2_unpack(fadd2(acc, f2_pack(p0, p1)), rsum[a], rsum[4 + a]);
@@ -799,6 +801,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         rs = ((rsum[0] + rsum[1]) + (rsum[2] + rsum[3])) + ((rsum[4] + rsum[5]) + (rsum[6] + rsum[7]));
         if constexpr (!kChunked) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pws[c][i] = pack_bf16x2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
           // P_t and O_t are free once PV_t(j-1) has completed
           if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], (j - 1) & 1, abort, prm.status))) {
             ok = false;
@@ -806,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) chunk_out(c);
+          for (int c = 0; c < 4; ++c) tmem_st16(tmem + lane_addr + p_col + c * 16, pws[c]);
         }
       } else if constexpr (C::kSepP) {
         // fast path passed: P goes to its own columns once PV_t(j-1) has read
@@ -817,13 +824,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pw[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pw[i] = pack_bf16x2(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
-          tmem_st16(tmem + lane_addr + p_col + c * 16, pw);
-        }
+        for (int c = 0; c < 4; ++c) tmem_st16(tmem + lane_addr + p_col + c * 16, pws[c]);
       }
 #undef SV
       __syncwarp();
