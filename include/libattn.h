@@ -238,11 +238,13 @@ attn_status kv_append(const attn_kv_cache *cache, const int32_t *block_table, in
  *   workspace >= paged_decode_workspace_size(batch, Hq, max_blocks,
  *              block_size, head_dim) bytes: split-K partials, linear in
  *              the longest possible context, never quadratic, and one split
- *              count per (sequence, KV head).  The counts must start at
- *              zero (the zero-fill before first use) and every call leaves
- *              them at zero: the CTA that finishes a (sequence, KV head)
- *              last merges its splits, so the call is a single launch.
- *              Calls that share a workspace must not overlap on the GPU.
+ *              count per (sequence, KV head): the CTA that finishes a
+ *              (sequence, KV head) last merges its splits, so the call is a
+ *              single launch.  Each call tags its counts with a generation
+ *              of its own, so they need no clearing between calls, shapes
+ *              or other uses of the buffer (only the status word must start
+ *              at zero).  Calls that share a workspace must not overlap on
+ *              the GPU.
  * Hq % Hkv == 0, Hq / Hkv <= 8.
  */
 attn_status paged_decode_attn(const attn_tensor *q, const attn_kv_cache *cache,

@@ -4,6 +4,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "libattn.h"
 
@@ -360,6 +362,17 @@ attn_status paged_kv_gather(const attn_kv_cache* cache, int32_t which, const int
   return from_cuda(launch_paged_gather(a, stream));
 }
 
+// Every decode call tags its split counts with a generation of its own, so a
+// workspace needs no clearing between calls, shapes or other uses (zero is
+// skipped: a zero-filled word then always belongs to no call).
+static std::atomic<uint32_t> g_decode_gen{0};
+
+static uint32_t next_decode_gen() {
+  uint32_t g = g_decode_gen.fetch_add(1, std::memory_order_relaxed) + 1;
+  if (g == 0) g = g_decode_gen.fetch_add(1, std::memory_order_relaxed) + 1;
+  return g;
+}
+
 static attn_status paged_decode_impl(const attn_tensor* q, const attn_tensor* k_new, const attn_tensor* v_new,
                                      const PagedCache& pc, const int32_t* block_table, int64_t bt_stride,
                                      int32_t max_blocks, const int32_t* lens_or_pos, float scale,
@@ -417,6 +430,7 @@ static attn_status paged_decode_impl(const attn_tensor* q, const attn_tensor* k_
   a.scale = scale;
   a.partials = static_cast<uint8_t*>(workspace) + kStatusBytes;
   a.n_split = decode_num_splits(max_blocks, pc.block_size);
+  a.gen = next_decode_gen();
   a.status = static_cast<uint32_t*>(workspace);
   return from_cuda(launch_paged_decode(a, stream));
 }

@@ -41,8 +41,11 @@ int decode_num_splits(int max_blocks, int block_size) {
 
 size_t decode_partial_bytes(int64_t B, int64_t Hq, int n_split, int D) {
   const size_t n = static_cast<size_t>(B) * Hq * n_split;
-  // outputs, log2 LSEs, and one split count per (sequence, KV head) (Hq bounds Hkv)
-  size_t bytes = n * D * sizeof(float) + n * sizeof(float) + static_cast<size_t>(B) * Hq * sizeof(int);
+  // outputs, log2 LSEs, and one 8-byte split count per (sequence, KV head)
+  // (Hq bounds Hkv), 8-byte aligned
+  size_t bytes = n * D * sizeof(float) + n * sizeof(float);
+  bytes = (bytes + 7) & ~size_t(7);
+  bytes += static_cast<size_t>(B) * Hq * sizeof(unsigned long long);
   return (bytes + 255) & ~size_t(255);
 }
 
@@ -51,7 +54,9 @@ SplitMerge decode_split_merge(const DecodeArgs& a, int D) {
   const size_t n = static_cast<size_t>(a.B) * a.Hq * a.n_split;
   m.o_part = static_cast<float*>(a.partials);
   m.lse_part = m.o_part + n * D;
-  m.count = reinterpret_cast<int*>(m.lse_part + n);
+  const size_t cnt_off = ((n * D + n) * sizeof(float) + 7) & ~size_t(7);
+  m.count = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(a.partials) + cnt_off);
+  m.gen = a.gen;
   m.n_split = a.n_split;
   m.Hq = static_cast<int>(a.Hq);
   m.Hkv = a.cache.Hkv;

@@ -14,13 +14,16 @@ namespace attn {
 // (sequence b, KV head gkv, 1024-token range); it writes its normalised
 // output and log2 LSE for each query head h = gkv * G + hh to
 //     o_part[((b * Hq + h) * n_split + split) * D + d],  lse_part[same slot]
-// and counts itself in count[b * Hkv + gkv].  The count starts at zero (the
-// workspace is zero-filled before its first use) and the merging CTA sets it
-// back to zero, so every call leaves it as it found it.
+// and counts itself in count[b * Hkv + gkv], a 64-bit word holding the
+// call's generation (high half) and the splits done (low half).  Every call
+// has a generation of its own, so a word from another call -- or whatever
+// the workspace held -- reads as zero splits done: the counts need no
+// initialisation and no reset.
 struct SplitMerge {
   float* o_part;    // [B, Hq, n_split, D]
   float* lse_part;  // [B, Hq, n_split], log2 units
-  int* count;       // [B, Hkv] splits done, per (sequence, KV head)
+  unsigned long long* count;  // [B, Hkv] (generation << 32) | splits done
+  uint32_t gen;     // this call's generation
   int n_split;
   int Hq, Hkv;
   void* out;        // [B, Hq, D] bf16 or f32, row strides os0 (batch), os1 (head) in elements
@@ -132,17 +135,26 @@ __device__ __forceinline__ void decode_merge_head(const SplitMerge& sm, int b, i
 // brings the count of (b, gkv) to ns (the splits that hold tokens), merge the
 // splits of the group's G heads (warp w takes heads w, w + NW, ...).  Every
 // CTA publishes its partial before its count (the fence), and the merging CTA
-// fences again before it reads the others'.  Called by all NW * 32 threads.
+// fences again before it reads the others'.  A word of another generation,
+// or one already at ns (the same generation replayed, as from a captured
+// graph), starts the count afresh.  Called by all NW * 32 threads.
 template <int D, int G, int NW>
 __device__ __forceinline__ void decode_finish(const SplitMerge& sm, int gkv, int b, int ns) {
   __shared__ int s_last;
   __syncthreads();  // every thread of the CTA has written its part of the partial
   if (threadIdx.x == 0) {
     __threadfence();
-    int* c = sm.count + static_cast<int64_t>(b) * sm.Hkv + gkv;
-    const bool last = atomicAdd(c, 1) == ns - 1;
-    if (last) atomicExch(c, 0);  // every split has counted: ready for the next call
-    s_last = last;
+    unsigned long long* c = sm.count + static_cast<int64_t>(b) * sm.Hkv + gkv;
+    const unsigned long long tag = static_cast<unsigned long long>(sm.gen) << 32;
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(c), now;
+    for (;;) {
+      const bool fresh = (old >> 32) == sm.gen && (old & 0xffffffffull) < static_cast<unsigned long long>(ns);
+      now = fresh ? old + 1 : tag + 1;
+      const unsigned long long seen = atomicCAS(c, old, now);
+      if (seen == old) break;
+      old = seen;
+    }
+    s_last = (now & 0xffffffffull) == static_cast<unsigned long long>(ns);
   }
   __syncthreads();
   if (!s_last) return;

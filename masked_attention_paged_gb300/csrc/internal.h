@@ -109,6 +109,7 @@ struct DecodeArgs {
   float scale;
   void* partials;  // workspace after the status block
   int n_split;     // split slots per (sequence, head) in the partial buffer
+  uint32_t gen;    // this call's generation, tags its split counts (never 0)
   uint32_t* status;
 };
 // tokens per split-K work unit of the paged decode

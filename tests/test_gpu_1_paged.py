@@ -123,8 +123,8 @@ def test_paged_decode_long_context():
 def test_paged_decode_reuses_its_workspace(D):
     """Three decode calls through one workspace with different context
     lengths (so each sequence has a different number of splits every time):
-    the split counts that the merging CTA resets must be back at zero for the
-    next call, and every call matches the oracle."""
+    each call's split counts start afresh under its own generation, and every
+    call matches the oracle."""
     cfg = workloads.DecodeConfig("w", 5, 8, 2, D, 16, 0, 3000, 4)
     d = workloads.make_decode_inputs(cfg, seed=89, ctx=[3000, 2500, 1024, 700, 5])
     ek, ev = oracle.kv_append(d.k_cache, d.v_cache, d.block_table, d.pos, d.k_new, d.v_new)
@@ -141,6 +141,40 @@ def test_paged_decode_reuses_its_workspace(D):
         ro, rl = oracle.paged_decode(d.q, kc, vc, d.block_table, lens, d.scale)
         assert_out_close(out, ro, what=f"reused workspace, lens {lens.tolist()}")
         assert_lse_close(lse, rl)
+
+
+def test_paged_decode_workspace_contents_do_not_matter():
+    """The split counts carry each call's generation, so a decode workspace
+    needs no clearing: filled with 0x7F bytes, with random bytes, or left
+    with the partials of a call of another shape (a larger batch, longer
+    contexts), it gives the oracle's result each time (only the status word
+    is reset)."""
+    cfg = workloads.DecodeConfig("z", 3, 8, 2, 128, 16, 0, 2100, 4)
+    d = workloads.make_decode_inputs(cfg, seed=90, ctx=[2100, 900, 40])
+    big = workloads.make_decode_inputs(workloads.DecodeConfig("zb", 9, 16, 2, 128, 16, 0, 4000, 4), seed=91,
+                                       ctx=[4000, 3900, 10, 2048, 1025, 3000, 5, 1, 2500])
+
+    def run(inp, ws):
+        ek, ev = oracle.kv_append(inp.k_cache, inp.v_cache, inp.block_table, inp.pos, inp.k_new, inp.v_new)
+        kc, vc = torch.from_numpy(ek).view(torch.bfloat16), torch.from_numpy(ev).view(torch.bfloat16)
+        out = lib.paged_decode_attn(inp.q.to(DEV), kc.to(DEV), vc.to(DEV), inp.block_table.to(DEV),
+                                    inp.ctx_lens.to(DEV), inp.scale, workspace=ws)
+        assert ws.status() == 0
+        ro, _ = oracle.paged_decode(inp.q, kc, vc, inp.block_table, inp.ctx_lens, inp.scale)
+        assert_out_close(out, ro, what=f"decode {inp.cfg.name}")
+
+    need = max(lib.paged_decode_workspace_size(x.cfg.B, x.cfg.Hq, x.block_table.shape[1], 16, 128) for x in (d, big))
+    ws = lib.Workspace(need)
+    ws.tensor.fill_(0x7F)
+    ws.reset()
+    run(d, ws)
+    g = torch.Generator(device="cpu").manual_seed(92)
+    ws.tensor.copy_(torch.randint(0, 256, ws.tensor.shape, generator=g, dtype=torch.uint8))
+    ws.reset()
+    run(d, ws)
+    run(big, ws)  # another shape: its partials now lie where the small call keeps its counts
+    run(d, ws)
+    run(big, ws)
 
 
 @pytest.mark.parametrize("D", [128, 64])
