@@ -101,7 +101,7 @@ def _decode_and_check(d: workloads.DecodeInputs, seed_note=""):
     return out
 
 
-@pytest.mark.parametrize("D,G", [(128, 4), (128, 1), (128, 8), (64, 4), (64, 2)])
+@pytest.mark.parametrize("D,G", [(128, 4), (128, 1), (128, 2), (128, 8), (64, 4), (64, 2), (64, 1), (64, 8)])
 def test_paged_decode_small(D, G):
     Hkv = 2
     cfg = workloads.DecodeConfig("s", 9, G * Hkv, Hkv, D, 16, 0, 1500, 4)

@@ -42,7 +42,8 @@ def _check(inp, causal, out_dtype=torch.bfloat16, note=""):
 
 
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("D,G,T", [(128, 4, 300), (128, 1, 37), (64, 4, 256), (64, 2, 1), (128, 8, 129)])
+@pytest.mark.parametrize("D,G,T", [(128, 4, 300), (128, 1, 37), (128, 2, 200), (64, 4, 256), (64, 2, 1), (64, 8, 150),
+                                   (64, 1, 300), (128, 8, 129)])
 def test_prefill_small(D, G, T, causal):
     """Starts 0 (a whole prompt), mid-block, on a tile edge, one past it, and
     long; chunks that end mid-block and mid-tile."""

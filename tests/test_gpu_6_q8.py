@@ -41,7 +41,7 @@ def _append_decode_check(d, note=""):
     assert_lse_close(lse, rl, what="q8 decode lse" + note)
 
 
-@pytest.mark.parametrize("D,G", [(128, 4), (128, 1), (128, 2), (128, 8), (64, 4), (64, 2)])
+@pytest.mark.parametrize("D,G", [(128, 4), (128, 1), (128, 2), (128, 8), (64, 4), (64, 2), (64, 1), (64, 8)])
 def test_q8_append_and_decode_small(D, G):
     Hkv = 2
     cfg = workloads.DecodeConfig("q", 9, G * Hkv, Hkv, D, 16, 0, 1500, 4)
