@@ -64,15 +64,16 @@ def test_workspace_sizes(L):
     assert L.attn_fwd_workspace_size_for(1, 24, 16380, 128) == 256
     assert L.attn_fwd_workspace_size_for(1, 16, -1, 64) == 0
     assert L.kv_append_workspace_size() == 256
-    # decode: status block + partials [B, Hq, n_split, D] + lse [B, Hq, n_split], split = 1024 tokens
+    # decode: status block + partials [B, Hq, n_split, D] + lse [B, Hq, n_split], split = 1024 tokens,
+    # then 8-byte split counts (B * Hq of them bound the B * Hkv used) at an 8-byte boundary
     n_split = -(-513 * 16 // 1024)
     assert n_split == 9
     part = 64 * 32 * n_split * (128 + 1) * 4
+    part = (part + 7) // 8 * 8 + 64 * 32 * 8
     assert L.paged_decode_workspace_size(64, 32, 513, 16, 128) == 256 + (part + 255) // 256 * 256
     # linear in the longest context, never quadratic
-    a = L.paged_decode_workspace_size(8, 32, 1024, 16, 128)
-    b = L.paged_decode_workspace_size(8, 32, 2048, 16, 128)
-    assert abs((b - 256) - 2 * (a - 256)) <= 256
+    a, b, c = (L.paged_decode_workspace_size(8, 32, m, 16, 128) for m in (1024, 2048, 3072))
+    assert abs((c - b) - (b - a)) <= 256 and c > b > a
 
 
 def _t(shape, dtype=1, stride=None, data=FAKE):
