@@ -773,9 +773,10 @@ def main():
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "inputs larger than L2: every step streams >1 GB (chunked inputs 604 MB, KV cache 1.2 GB)",
                    "decode_kv_gbs": rows["paged_decode_attn"]["kv_gbs"]},
-        "roofline": {"bound": "tensor", "kernel": "attn_fwd_tc_kernel<D=128> (chunked workload, 2 launches/step)",
+        "roofline": {"bound": "tensor",
+                     "kernel": "attn_fwd_pair_kernel (D=128 on CTA pairs; chunked workload, 2 launches/step)",
                      "achieved": chunk_tflops, "peak": peak_t, "unit": "TFLOP/s", "frac": chunk_tflops / peak_t,
-                     "traffic": traffic("attn_fwd_tc_kernel"),
+                     "traffic": traffic("attn_fwd_pair_kernel"),
                      "peak_source": (f"{pk['source']} bf16 burst GEMM rate (the step runs ~13 ms at a time at the "
                                      f"burst clock: median {mhz} MHz sampled here; the sustained figure "
                                      f"{pk['bf16_tflops_sustained']} was taken at {pk['gemm_sm_mhz']} MHz)"),

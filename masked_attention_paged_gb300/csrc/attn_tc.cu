@@ -1030,12 +1030,43 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// The slots of make_tile_map, as attn_tc_kernel reads them.
+bool make_map(CUtensorMap* map, TmaCoordMap* cm, const View4& t) {
+  int slot[3];
+  if (!make_tile_map(map, slot, t, kBM)) return false;
+  cm->slot_p = slot[0];
+  cm->slot_h = slot[1];
+  cm->slot_b = slot[2];
+  return true;
+}
+
+// A 4-D bf16 tensor map over one paged cache tensor [num_blocks, Hkv, 16, D]
+// (contiguous): dims (D, slot, head, block), box 64 columns x 16 slots of one
+// head of one block, 128-byte swizzle.
+bool make_cache_map(CUtensorMap* map, void* base, int64_t num_blocks, int Hkv, int D) {
+  EncodeTiledFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), 16, static_cast<cuuint64_t>(Hkv),
+                              static_cast<cuuint64_t>(num_blocks)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(16) * D * 2,
+                                 static_cast<cuuint64_t>(Hkv) * 16 * D * 2};
+  const cuuint32_t box[4] = {64, 16, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 // A 4-D bf16 tensor map over a [B, H, P, D] view whose row/head/batch
 // strides may come in any order (contiguous or packed [T, H, D]).  The
-// three outer dimensions are ordered by increasing stride; `cm` records which
-// coordinate slot carries which index.  Box: 64 columns x 128 rows, 128-byte
+// three outer dimensions are ordered by increasing stride; slot[0], slot[1]
+// and slot[2] receive the coordinate slot (1..3) that carries the row, the
+// head and the batch index.  Box: 64 columns x box_rows rows, 128-byte
 // swizzle, zero fill outside the tensor.
-bool make_map(CUtensorMap* map, TmaCoordMap* cm, const View4& t) {
+bool make_tile_map(CUtensorMap* map, int slot[3], const View4& t, int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (enc == nullptr) return false;
   struct Dim {
@@ -1059,40 +1090,14 @@ bool make_map(CUtensorMap* map, TmaCoordMap* cm, const View4& t) {
   for (int i = 0; i < 3; ++i) {
     dims[i + 1] = static_cast<cuuint64_t>(d[i].size < 1 ? 1 : d[i].size);
     strides[i] = static_cast<cuuint64_t>(d[i].stride) * 2;
-    if (d[i].which == 0) {
-      box[i + 1] = kBM;
-      cm->slot_p = i + 1;
-    } else if (d[i].which == 1) {
-      cm->slot_h = i + 1;
-    } else {
-      cm->slot_b = i + 1;
-    }
+    slot[d[i].which] = i + 1;
+    if (d[i].which == 0) box[i + 1] = static_cast<cuuint32_t>(box_rows);
   }
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t.data, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
-
-// A 4-D bf16 tensor map over one paged cache tensor [num_blocks, Hkv, 16, D]
-// (contiguous): dims (D, slot, head, block), box 64 columns x 16 slots of one
-// head of one block, 128-byte swizzle.
-bool make_cache_map(CUtensorMap* map, void* base, int64_t num_blocks, int Hkv, int D) {
-  EncodeTiledFn enc = encode_fn();
-  if (enc == nullptr) return false;
-  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), 16, static_cast<cuuint64_t>(Hkv),
-                              static_cast<cuuint64_t>(num_blocks)};
-  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(16) * D * 2,
-                                 static_cast<cuuint64_t>(Hkv) * 16 * D * 2};
-  const cuuint32_t box[4] = {64, 16, 1, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-}  // namespace
 
 bool make_bf16_cache_map(CUtensorMap* map, void* base, int64_t num_blocks, int Hkv) {
   return make_cache_map(map, base, num_blocks, Hkv, 128);
@@ -1183,12 +1188,8 @@ cudaError_t launch_tc(const AttnFwdArgs& a, cudaStream_t stream) {
   kern<<<static_cast<unsigned>(ctas), kThreads, smem, stream>>>(mq, mk, mv, p);
   e = cudaGetLastError();
   if (e != cudaSuccess || p.split == 1) return e;
-  const int tail_units = static_cast<int>(units - p.full_units);
-  const int64_t threads = static_cast<int64_t>(tail_units) * (2 * kBM) * 32;
-  split_merge_kernel<D, OUT_BF16><<<static_cast<unsigned>((threads + 255) / 256), 256, 0, stream>>>(
-      p.part_o, p.part_lse, p.split, p.full_units, tail_units, p.nq, p.Hq, p.Pq, a.out.data, a.out.stride[0],
-      a.out.stride[1], a.out.stride[2], a.lse);
-  return cudaGetLastError();
+  return launch_split_merge(D, OUT_BF16, p.part_o, p.part_lse, p.split, p.full_units,
+                            static_cast<int>(units - p.full_units), p.nq, p.Hq, p.Pq, a.out, a.lse, stream);
 }
 
 template <int D, bool OUT_BF16>
@@ -1248,8 +1249,37 @@ size_t split_partial_bytes(int D) {
   return sms * (2 * kBM) * (static_cast<size_t>(D) + 1) * sizeof(float);
 }
 
+cudaError_t launch_split_merge(int D, bool out_bf16, const float* part_o, const float* part_lse, int split,
+                               int full_units, int tail, int nq, int Hq, int Pq, const View4& out, float* lse,
+                               cudaStream_t stream) {
+  const int64_t threads = static_cast<int64_t>(tail) * (2 * kBM) * 32;
+  const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
+  const int64_t s0 = out.stride[0], s1 = out.stride[1], s2 = out.stride[2];
+  if (D == 64 && out_bf16)
+    split_merge_kernel<64, true><<<blocks, 256, 0, stream>>>(part_o, part_lse, split, full_units, tail, nq, Hq, Pq,
+                                                             out.data, s0, s1, s2, lse);
+  else if (D == 64)
+    split_merge_kernel<64, false><<<blocks, 256, 0, stream>>>(part_o, part_lse, split, full_units, tail, nq, Hq, Pq,
+                                                              out.data, s0, s1, s2, lse);
+  else if (D == 128 && out_bf16)
+    split_merge_kernel<128, true><<<blocks, 256, 0, stream>>>(part_o, part_lse, split, full_units, tail, nq, Hq,
+                                                              Pq, out.data, s0, s1, s2, lse);
+  else if (D == 128)
+    split_merge_kernel<128, false><<<blocks, 256, 0, stream>>>(part_o, part_lse, split, full_units, tail, nq, Hq,
+                                                               Pq, out.data, s0, s1, s2, lse);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attn_fwd_tc(const AttnFwdArgs& a, cudaStream_t stream) {
   const bool bf16_out = a.out.dtype == ATTN_BF16;
+  if (pair_kernel_applies(a)) {
+    // D = 128 without a mask: the CTA-pair kernel, where the device can
+    // hold its clusters
+    const cudaError_t e = launch_attn_fwd_pair(a, stream);
+    if (e != cudaErrorNotSupported) return e;
+  }
   if (a.D == 64) {
     // with key bounds: P apart from S and the certified max-free tiles;
     // without: P over S and the optimistic tiles

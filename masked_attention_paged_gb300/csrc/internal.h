@@ -33,6 +33,18 @@ struct AttnFwdArgs {
 
 // bf16 inputs, D in {64, 128}: tcgen05 + TMA kernel
 cudaError_t launch_attn_fwd_tc(const AttnFwdArgs& a, cudaStream_t stream);
+// D = 128, no mask, no key lengths, scale > 0: the kernel on CTA pairs;
+// cudaErrorNotSupported when the call or the device does not allow it
+bool pair_kernel_applies(const AttnFwdArgs& a);
+cudaError_t launch_attn_fwd_pair(const AttnFwdArgs& a, cudaStream_t stream);
+// bf16 tensor map over a [B, H, P, D] view: box 64 columns x box_rows rows,
+// 128-byte swizzle; slot[0..2] = coordinate slot of the row, head, batch
+bool make_tile_map(CUtensorMap* map, int slot[3], const View4& t, int box_rows);
+// merge the key parts of the split last-wave units of a tensor-core launch
+// (256-row units, `split` parts each, normalised f32 rows + natural-log LSEs)
+cudaError_t launch_split_merge(int D, bool out_bf16, const float* part_o, const float* part_lse, int split,
+                               int full_units, int tail, int nq, int Hq, int Pq, const View4& out, float* lse,
+                               cudaStream_t stream);
 // f32 inputs, D <= 128, D % 4 == 0: FFMA kernel
 cudaError_t launch_attn_fwd_simt(const AttnFwdArgs& a, cudaStream_t stream);
 // Pk == 0: out = 0, lse = -inf
