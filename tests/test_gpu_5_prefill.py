@@ -105,8 +105,12 @@ def test_chunked_prefill_equals_whole_prompt_on_gpu():
     assert (l2 - lw[:, :, S:]).abs().max().item() <= 1e-3
 
 
-def test_prefill_bad_start_and_bad_block():
-    cfg = workloads.PrefillConfig("b", 3, 8, 2, 64, 50, 16, 0, 0, 2, True)
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_bad_start_and_bad_block(D):
+    """A start position past the table and a block id outside the cache are
+    reported, the sequence concerned is written as zeros, the others are
+    exact (D 128 runs on CTA pairs, D 64 on the one-CTA kernel)."""
+    cfg = workloads.PrefillConfig("b", 3, 8, 2, D, 50, 16, 0, 0, 2, True)
     inp = workloads.make_prefill_inputs(cfg, seed=24, start=[10, 20, 30])
     g = _dev(inp)
     sp = g["start_pos"].clone()
